@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV decode hot path on GB300.
+
+A step is one pass of the whole hot path over one batch: the cache write of
+every sequence's new token (pa_reshape_and_cache), the copy-on-write block
+copies when the workload has any (pa_copy_blocks), and paged decode
+attention over the pool (pa_decode: main kernel + log-sum-exp reduce).
+
+Default workload: a Qwen2.5-7B-like decode layer -- 28 query / 4 KV heads,
+head_dim 128, block 16, fp16 KV, batch 64 with lengths uniform in [100, 8192]
+over a shuffled 40,000-block pool (0.54 GB of K+V, larger than the 129 MB L2,
+so every step streams the pool from HBM).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs the full
+workload on its own GPU (independent sequences, no data exchange: weak
+scaling); the value is all ranks' tokens over the slowest rank's time.
+``--impl reference`` times the CPU oracle (the plain single-threaded
+restatement of the pages' method) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention tokens/s and achieved KV HBM GB/s (% of 8 TB/s) on 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def make_workload(name: str, seed: int, device: str):
+    from paged_kv_cache_69_gb300 import inputs
+    gd = device
+    table = {
+        "qwen7b_fp16": lambda: inputs.qwen7b_fp16(seed=seed, gen_device=gd),
+        "short_mix_bf16_bs16": lambda: inputs.short_mix_bf16(seed=seed + 1, block_size=16, gen_device=gd),
+        "short_mix_bf16_bs8": lambda: inputs.short_mix_bf16(seed=seed + 1, block_size=8, gen_device=gd),
+        "prefix_share_fp16": lambda: inputs.prefix_share_fp16(seed=seed + 2, prompt_len=2048, gen_device=gd),
+        "prefix_share_cow_fp16": lambda: inputs.prefix_share_fp16(seed=seed + 2, prompt_len=2040, gen_device=gd),
+        "long_ctx_bf16": lambda: inputs.long_ctx("bf16", seed=seed + 3, gen_device=gd),
+        "long_ctx_fp8": lambda: inputs.long_ctx("fp8_e4m3", seed=seed + 3, gen_device=gd),
+        "tiny_fp32": lambda: inputs.tiny_fp32(seed=seed - 1),
+    }
+    return table[name]()
+
+
+def workload_config(wl, extra=None) -> dict:
+    cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+           "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+           "num_blocks": wl.num_blocks, "kv_dtype": wl.kv_dtype, "q_dtype": wl.q_dtype,
+           "total_tokens": int(wl.seq_lens.sum()), "max_seq_len": int(wl.seq_lens.max())}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_69_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, when it was taken from the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"pa_decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    s = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if m and s and s.group(1) == source_digest():
+        return int(m.group(1))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML read-only queries)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, interval_s: float = 0.005):
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self._interval = interval_s
+        try:
+            import torch
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+                if self.nvml.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.handle)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _sample(self):
+        mhz = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        r1 = self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz))
+        r2 = self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle, ctypes.byref(reasons))
+        if r1 == 0:
+            self.samples.append((int(mhz.value), int(reasons.value) if r2 == 0 else 0))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self._interval)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self) -> dict | None:
+        if not self.ok:
+            return None
+        self._stop.set()
+        self._thread.join()
+        if not self.samples:
+            self._sample()
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if bits & b], "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_inputs(wl):
+    import oracle
+    k = oracle.as_raw(wl.k_cache).copy()
+    v = oracle.as_raw(wl.v_cache).copy()
+    return k, v
+
+
+def oracle_step(wl, k, v, seqs):
+    """The oracle's cache write of the sampled sequences' new tokens, then
+    their decode attention over every query head."""
+    import numpy as np
+    import oracle
+    kvd, sd = oracle.DTYPE_CODES[wl.kv_dtype], oracle.DTYPE_CODES[wl.src_dtype]
+    idx = np.array(seqs)
+    oracle.reshape_and_cache(k, v, kvd, oracle.as_raw(wl.new_key)[idx], oracle.as_raw(wl.new_value)[idx], sd,
+                             oracle.as_raw(wl.slot_mapping)[idx], wl.num_kv_heads, wl.head_dim,
+                             wl.block_size, wl.num_blocks, wl.k_scale, wl.v_scale)
+    prob = oracle.Problem(wl.q, oracle.DTYPE_CODES[wl.q_dtype], k, v, kvd, wl.block_tables, wl.seq_lens,
+                          wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, wl.num_blocks,
+                          wl.scale, wl.k_scale, wl.v_scale)
+    for i in seqs:
+        for h in range(wl.num_q_heads):
+            oracle.attend_one(prob, i, h)
+
+
+def time_oracle(wl, budget_s: float = 15.0):
+    """Sequences per second of the oracle over a bounded sample: sequences in
+    workload order until ~budget_s of CPU work."""
+    k, v = oracle_inputs(wl)
+    done, t0 = [], time.perf_counter()
+    for i in range(wl.num_seqs):
+        oracle_step(wl, k, v, [i])
+        done.append(i)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return len(done) / el, len(done), el
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args) -> dict:
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = make_workload(args.workload, 1, dev)
+    wl = wl.to("cpu")
+    k, v = oracle_inputs(wl)
+    # a step: the oracle on a bounded sample of the workload (as many
+    # sequences as fit in ~1.5 s, measured on the first one)
+    t0 = time.perf_counter()
+    oracle_step(wl, k, v, [0])
+    one = time.perf_counter() - t0
+    per_step = max(1, min(wl.num_seqs, int(1.5 / max(one, 1e-6))))
+    seqs = list(range(per_step))
+    for _ in range(args.warmup):
+        oracle_step(wl, k, v, seqs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, k, v, seqs)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    sample = (f"first {per_step} of {wl.num_seqs} sequences per step (all {wl.num_q_heads} query heads, "
+              f"cache write + decode), oracle in plain C, one thread")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl, {"sample_seqs_per_step": per_step}),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, rank, world, local) -> dict | None:
+    import torch
+    import torch.distributed as dist
+    import paged_kv_cache_69_gb300 as pa
+    from paged_kv_cache_69_gb300 import sizing
+
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    pa.build()
+    wl = make_workload(args.workload, 1, device)
+    d = wl.to(device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    for kind, payload in d.setup:
+        if kind == "copy":
+            pa.pa_copy_blocks(d.k_cache, d.v_cache, payload, err_flag=err)
+        else:
+            pa.pa_reshape_and_cache(d.k_cache, d.v_cache, payload.key, payload.value, payload.slots,
+                                    k_scale=d.k_scale, v_scale=d.v_scale, err_flag=err)
+    out = torch.empty_like(d.q)
+    MB = d.block_tables.shape[1]
+    ws = pa.alloc_workspace(d.num_seqs, d.num_q_heads, d.head_dim, MB * d.block_size, args.partition_tokens,
+                            device=device)
+    stream = torch.cuda.current_stream()
+    pairs = d.cow_pairs if (d.cow_pairs is not None and d.cow_pairs.numel()) else None
+
+    def write(q_, key_, val_, slots_):
+        pa.pa_reshape_and_cache(d.k_cache, d.v_cache, key_, val_, slots_, k_scale=d.k_scale,
+                                v_scale=d.v_scale, err_flag=err)
+
+    def decode(q_, bt_, sl_, out_):
+        pa.pa_decode(out_, q_, d.k_cache, d.v_cache, bt_, sl_, d.scale, k_scale=d.k_scale, v_scale=d.v_scale,
+                     partition_tokens=args.partition_tokens, workspace=ws, err_flag=err, simt=args.simt)
+
+    def step(q_, key_, val_, slots_, bt_, sl_, out_):
+        if pairs is not None:
+            pa.pa_copy_blocks(d.k_cache, d.v_cache, pairs, err_flag=err)
+        write(q_, key_, val_, slots_)
+        decode(q_, bt_, sl_, out_)
+
+    dev_args = (d.q, d.new_key, d.new_value, d.slot_mapping, d.block_tables, d.seq_lens, out)
+    for _ in range(args.warmup):
+        step(*dev_args)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    t_start.record(stream)
+    for i in range(K):
+        if pairs is not None:
+            pa.pa_copy_blocks(d.k_cache, d.v_cache, pairs, err_flag=err)
+        write(d.q, d.new_key, d.new_value, d.slot_mapping)
+        ev[i][0].record(stream)
+        decode(d.q, d.block_tables, d.seq_lens, out)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    t = torch.tensor([ms_total, dec_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total, dec_ms = float(t[0]), float(t[1])
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()} during the benchmark")
+
+    # ---- end to end: host buffers, copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        host = [x.cpu().pin_memory() for x in (d.q, d.new_key, d.new_value, d.slot_mapping, d.block_tables,
+                                                d.seq_lens)]
+        stage = [torch.empty_like(x) for x in (d.q, d.new_key, d.new_value, d.slot_mapping, d.block_tables,
+                                               d.seq_lens)]
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host)
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for s_, h_ in zip(stage, host):
+                s_.copy_(h_, non_blocking=True)
+            step(stage[0], stage[1], stage[2], stage[3], stage[4], stage[5], out)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device=device)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": wl.num_seqs * world * K / (float(te[0]) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        return None
+    lens = wl.seq_lens.tolist()
+    alg = sizing.decode_algorithmic_bytes(lens, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
+                                          wl.q_dtype)
+    if wl.meta.get("unique_tokens"):
+        # shared prefix blocks are read once from HBM: count each unique token once
+        alg = (wl.meta["unique_tokens"] * wl.num_kv_heads * wl.head_dim * sizing.ELEM_BYTES[wl.kv_dtype] * 2 +
+               wl.num_seqs * wl.num_q_heads * wl.head_dim * 2 * sizing.ELEM_BYTES[wl.q_dtype])
+    peak, peak_src = measured_peak()
+    achieved = alg / (dec_ms / 1e3) / 1e9
+    value = wl.num_seqs * world * K / (ms_total / 1e3)
+    res = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+           "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": wl.kv_dtype, "data": "synthetic",
+           "config": workload_config(wl, {"l2": "inputs larger than L2 (K+V pool streamed each step)",
+                                          "decode_variant": "cuda-core" if args.simt else "tensor-core",
+                                          "partition_tokens": args.partition_tokens,
+                                          "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
+           "kv_gbs": achieved, "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "peak_source": peak_src,
+                        "kernel": "pa_decode (main + reduce)", "algorithmic_bytes_per_launch": alg,
+                        "launch_ms": dec_ms, "traffic": profile_traffic(args.workload)},
+           "gpu_launches": K * (3 + (1 if pairs is not None else 0)),
+           "clocks": clk, "e2e": e2e}
+    if not args.no_cpu_baseline and world == 1:
+        rate, n, el = time_oracle(wl.to("cpu"), budget_s=args.cpu_budget)
+        res["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                               "sample": f"first {n} of {wl.num_seqs} sequences (all {wl.num_q_heads} query "
+                                         f"heads, cache write + decode), {el:.1f} s, one thread"}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen7b_fp16")
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--simt", action="store_true", help="time the CUDA-core decode variant")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local)
+    if res is not None:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * pa.h -- C interface of the GB300 paged-KV decode library (libpa.so).
+ *
+ * The library implements the data-parallel hot path of paged KV caching:
+ *   pa_reshape_and_cache  write new tokens' K/V into pool slots,
+ *   pa_copy_blocks        copy-on-write of shared blocks,
+ *   pa_decode             one decode step of attention over a paged pool.
+ *
+ * Layouts (row-major, innermost last):
+ *   k_cache, v_cache   [num_blocks, block_size, num_kv_heads, head_dim]
+ *                      one pool per layer, K and V separate
+ *                      ("kv-cache-memory-core", section 2.2).
+ *   block_tables       int32 [num_seqs, max_blocks_per_seq]; entry j of row i
+ *                      is the physical block holding tokens
+ *                      [j*block_size, (j+1)*block_size) of sequence i
+ *                      ("vLLM intro part 2", section 3.2).  Entries at or past
+ *                      cdiv(seq_lens[i], block_size) are never read.
+ *   seq_lens           int32 [num_seqs], tokens attended per sequence.
+ *   slot_mapping       int64 [num_tokens], absolute pool slot of each new
+ *                      token, block*block_size + offset (same section).
+ *   q, out             [num_seqs, num_q_heads, head_dim], one decode query
+ *                      per sequence; out has the type of q.
+ *   key, value         [num_tokens, num_kv_heads, head_dim].
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads)
+ *   ("kv-cache-memory-core", section 4.2, grouped-query attention).
+ *
+ * Ownership and execution: every pointer is a device pointer owned by the
+ * caller, including the workspace.  Every call is asynchronous on `stream`,
+ * allocates nothing and never synchronises the host.  Host-side argument
+ * checks return a status before anything is launched.  Out-of-range indices
+ * met on the device (a block id, a slot or a copy pair outside the pool, a
+ * sequence longer than its table) skip the affected unit and OR a bit into
+ * *err_flag (if err_flag is non-null); kernels never trap.  Identical inputs
+ * give bit-identical outputs (no floating-point atomics).
+ *
+ * Supported shapes: head_dim 64 or 128; block_size 8, 16 or 32;
+ * num_q_heads a multiple of num_kv_heads; num_kv_heads <= 256.
+ * Element types: f32 caches need f32 q; f16/bf16 caches need q of the same
+ * type; fp8-e4m3 caches take f16 or bf16 q (head_dim 128 only).
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shape */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not supported (dtype combo, head_dim, ...) */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    PA_ERR_CUDA = 4           /* a CUDA runtime/driver call failed; see pa_last_error_detail */
+} pa_status;
+
+typedef enum {
+    PA_F32 = 0,
+    PA_F16 = 1,
+    PA_BF16 = 2,
+    PA_FP8_E4M3 = 3           /* OCP E4M3 (finite-only, max 448), one byte */
+} pa_dtype;
+
+/* Bits OR-ed into *err_flag by device code. */
+#define PA_ERRBIT_BAD_BLOCK     1u   /* block table entry outside [0, num_blocks) */
+#define PA_ERRBIT_BAD_SLOT      2u   /* slot_mapping entry >= num_blocks*block_size */
+#define PA_ERRBIT_BAD_PAIR      4u   /* copy pair id outside [0, num_blocks) */
+#define PA_ERRBIT_SEQ_TOO_LONG  8u   /* seq_lens[i] < 0 or > max_blocks_per_seq*block_size */
+#define PA_ERRBIT_WAIT_TIMEOUT 16u   /* an internal pipeline wait exceeded its time limit */
+
+/* Human-readable name of a status. */
+const char* pa_status_string(pa_status s);
+
+/* Detail of the most recent failure on the calling host thread ("" if none). */
+const char* pa_last_error_detail(void);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs on the
+ * current device for these bounds.  max_seq_len bounds every seq_lens[i];
+ * partition_tokens is the value that will be passed to pa_decode.
+ * Returns 0 for invalid arguments.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                int max_seq_len, int partition_tokens);
+
+/*
+ * pa_decode -- single-query decode attention over a paged KV pool
+ * ("vLLM intro part 2", section 4 (kernel layer, the softmax and dot-product
+ * formulas); PagedAttention note (vagrantpi PKM), kernel steps: look up the
+ * block table, load block by block, merge across blocks with online softmax).
+ *
+ * For every sequence i and query head h, with g = h / (num_q_heads /
+ * num_kv_heads) and L = seq_lens[i]:
+ *   s_t   = scale * <q[i,h,:], K_t>            t in [0, L)
+ *   out   = sum_t softmax(s)_t * V_t
+ * where K_t, V_t are row (t % block_size, g) of physical block
+ * block_tables[i][t / block_size].  fp8 caches are dequantised in registers:
+ * K_t = e4m3(k) * k_scale, V_t = e4m3(v) * v_scale (scales ignored otherwise).
+ * L == 0 writes zeros.
+ *
+ * The work is split into 16-token chunks, balanced over persistent CTAs;
+ * sequences spanning several CTAs (or longer than partition_tokens) are
+ * merged afterwards by a log-sum-exp reduction kernel on the same stream.
+ *   partition_tokens  0 lets the library choose split points; otherwise a
+ *                     positive multiple of 16: sequences are additionally
+ *                     split every partition_tokens tokens.
+ *   workspace         device buffer of at least pa_decode_workspace_size(...)
+ *                     bytes, 256-byte aligned; contents need no initialisation
+ *                     and are scratch between calls.  Calls sharing one
+ *                     workspace must not overlap on the GPU.
+ *   err_flag          optional device int32 receiving PA_ERRBIT_* bits.
+ * Alignment: q, out, k_cache, v_cache must be 16-byte aligned.
+ */
+pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype,
+                    const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                    float scale, float k_scale, float v_scale,
+                    int partition_tokens, void* workspace, size_t workspace_bytes,
+                    int32_t* err_flag, cudaStream_t stream);
+
+/*
+ * pa_decode_simt -- the same operation, arguments and results as pa_decode,
+ * computed with CUDA-core FMAs instead of tensor-core MMAs.  It is the path
+ * for f32 caches and a measured comparison point for the others.
+ */
+pa_status pa_decode_simt(void* out, const void* q, pa_dtype q_dtype,
+                         const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, float k_scale, float v_scale,
+                         int partition_tokens, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, cudaStream_t stream);
+
+/*
+ * pa_reshape_and_cache -- write token t's K and V rows ([num_kv_heads,
+ * head_dim] each) into pool slot slot_mapping[t] ("vLLM intro part 2",
+ * section 3.2, slot_mapping; "kv-cache-memory-core", section 3, decode
+ * appends one slot per step).
+ *   slot < 0                          padding: skipped, no error.
+ *   slot >= num_blocks*block_size     skipped, PA_ERRBIT_BAD_SLOT.
+ * Same-type writes copy bits.  An fp8 cache quantises on write
+ * ("kv-cache-memory-core", section 4.4): byte = e4m3_satfinite_rne(x / scale)
+ * with x the source value widened to float, IEEE float division, round to
+ * nearest even, saturation to +-448; NaN becomes the NaN code.  Sources for
+ * an fp8 cache may be f32, f16 or bf16; other caches need src == kv dtype.
+ * Duplicate slots within one call leave one of the writes (unspecified which).
+ */
+pa_status pa_reshape_and_cache(void* k_cache, void* v_cache, pa_dtype kv_dtype,
+                               const void* key, const void* value, pa_dtype src_dtype,
+                               const int64_t* slot_mapping, int num_tokens,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, float k_scale, float v_scale,
+                               int32_t* err_flag, cudaStream_t stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write block copies ("vLLM intro part 2",
+ * section 5; aibook "显存与 KV 缓存", the copy-on-write steps: copy first,
+ * repoint the table, then write).  For each pair p, the whole K block and V
+ * block block_mapping[2p] are copied onto block block_mapping[2p+1].
+ * num_pairs == 0 is a no-op.  A pair with an id outside [0, num_blocks) is
+ * skipped with PA_ERRBIT_BAD_PAIR.  Destinations must be distinct and must
+ * not be the source of another pair in the same call.
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype kv_dtype,
+                         const int64_t* block_mapping, int num_pairs,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, int32_t* err_flag, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

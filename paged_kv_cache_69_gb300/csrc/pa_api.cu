@@ -1,0 +1,343 @@
+// pa_api.cu -- host side of pa_decode / pa_decode_simt: argument checks,
+// launch planning (heads per CTA, pipeline depth, persistent grid), TMA
+// tensor-map encoding, workspace carving and the two launches (main kernel,
+// then the log-sum-exp reduce kernel with programmatic dependent launch).
+// Also the status strings shared by every entry point.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pa_common.h"
+#include "pa_decode_kernel.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// status reporting
+// ---------------------------------------------------------------------------
+static thread_local char g_detail[256] = "";
+
+void clear_error() { g_detail[0] = '\0'; }
+
+pa_status fail(pa_status s, const char* what) {
+    std::snprintf(g_detail, sizeof g_detail, "%s", what);
+    return s;
+}
+
+pa_status fail_cuda(const char* what, cudaError_t e) {
+    std::snprintf(g_detail, sizeof g_detail, "%s: %s", what, cudaGetErrorString(e));
+    return PA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// device facts (cached per device)
+// ---------------------------------------------------------------------------
+struct DeviceInfo { int sms = 0; int max_smem = 0; };
+
+static bool device_info(DeviceInfo& info) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms == 0) {
+        int sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
+        cache[dev].sms = sms;
+        cache[dev].max_smem = smem;
+    }
+    info = cache[dev];
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// tensor-map encoding through the driver entry point
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+static CUtensorMapDataType tmap_type(pa_dtype d) {
+    switch (d) {
+        case PA_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        case PA_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        case PA_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    }
+}
+
+// One TMA box = `rpb` pool rows x HPC heads x the whole head_dim, placed in
+// shared memory as [column block of 128 B][head][row][128 B] with the 128-B
+// swizzle.  The 4-D map lists the dimensions in that shared-memory order
+// (column-in-block, row, head, column block), so one copy moves the box.
+// Fallback: a 3-D map in the pool's natural order, one copy per
+// (column block, head).
+static CUresult encode_kv_map(CUtensorMap* m, const void* cache, pa_dtype kvd, int NB, int bs, int Hkv,
+                              int D, int HPC, int rpb, bool per_head) {
+    const EncodeTiledFn enc = encode_fn();
+    if (!enc) return CUDA_ERROR_NOT_FOUND;
+    const int e = dtype_bytes(kvd);
+    const cuuint64_t rows = static_cast<cuuint64_t>(NB) * bs;
+    const cuuint32_t e128 = 128 / e;
+    const cuuint32_t DH = static_cast<cuuint32_t>(D * e / 128);
+    if (!per_head) {
+        cuuint64_t dims[4] = {e128, rows, static_cast<cuuint64_t>(Hkv), DH};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(Hkv) * D * e, static_cast<cuuint64_t>(D) * e, 128};
+        cuuint32_t box[4] = {e128, static_cast<cuuint32_t>(rpb), static_cast<cuuint32_t>(HPC), DH};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        return enc(m, tmap_type(kvd), 4, const_cast<void*>(cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv), rows};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(Hkv) * D * e};
+    cuuint32_t box[3] = {e128, 1, static_cast<cuuint32_t>(rpb)};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, tmap_type(kvd), 3, const_cast<void*>(cache), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// ---------------------------------------------------------------------------
+// launch planning
+// ---------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int cdiv_h(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+static size_t workspace_bytes_for(int B, int Hq, int D, int max_seq_len, int partition_tokens, int sms) {
+    const long long nr_cap = 2LL * sms;
+    const long long units = partition_tokens > 0 ? static_cast<long long>(B) * cdiv_h(max_seq_len, partition_tokens)
+                                                 : static_cast<long long>(B);
+    const long long slots = nr_cap + units;
+    return align256(sizeof(int2) * static_cast<size_t>(B)) + 256 +
+           align256(sizeof(float2) * static_cast<size_t>(slots) * Hq) +
+           align256(sizeof(float) * static_cast<size_t>(slots) * Hq * D);
+}
+
+static int max_slots_for(int B, int max_seq_len, int partition_tokens, int sms) {
+    const long long units = partition_tokens > 0 ? static_cast<long long>(B) * cdiv_h(max_seq_len, partition_tokens)
+                                                 : static_cast<long long>(B);
+    return static_cast<int>(std::min<long long>(2LL * sms + units, 0x7fffffffLL));
+}
+
+static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
+                             const void* v_cache, pa_dtype kv_dtype, const int32_t* block_tables, int MB,
+                             const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int bs, int NB,
+                             float scale, float k_scale, float v_scale, int partition_tokens,
+                             void* workspace, size_t workspace_bytes, int32_t* err_flag, cudaStream_t stream) {
+    clear_error();
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || bs <= 0 || NB <= 0 || MB <= 0)
+        return fail(PA_ERR_INVALID_ARG, "decode: sizes must be positive (num_seqs >= 0)");
+    if (B == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+        return fail(PA_ERR_INVALID_ARG, "decode: null pointer");
+    if (!valid_dtype(q_dtype) || !valid_dtype(kv_dtype)) return fail(PA_ERR_INVALID_ARG, "decode: unknown dtype");
+    if (Hq % Hkv != 0) return fail(PA_ERR_INVALID_ARG, "decode: num_q_heads must be a multiple of num_kv_heads");
+    if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "decode: head_dim must be 64 or 128");
+    if (bs != 8 && bs != 16 && bs != 32) return fail(PA_ERR_UNSUPPORTED, "decode: block_size must be 8, 16 or 32");
+    if (Hkv > 256) return fail(PA_ERR_UNSUPPORTED, "decode: num_kv_heads must be <= 256");
+    if (partition_tokens < 0 || partition_tokens % 16 != 0)
+        return fail(PA_ERR_INVALID_ARG, "decode: partition_tokens must be 0 or a positive multiple of 16");
+    if (static_cast<long long>(NB) * bs >= (1LL << 31) || static_cast<long long>(MB) * bs >= (1LL << 30))
+        return fail(PA_ERR_UNSUPPORTED, "decode: pool or table too large for 32-bit row coordinates");
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "decode: q, out, k_cache and v_cache must be 16-byte aligned");
+    if (kv_dtype == PA_FP8_E4M3) {
+        if (q_dtype != PA_F16 && q_dtype != PA_BF16)
+            return fail(PA_ERR_UNSUPPORTED, "decode: an fp8 cache needs f16 or bf16 queries");
+        if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite_host(k_scale) || !isfinite_host(v_scale))
+            return fail(PA_ERR_INVALID_ARG, "decode: fp8 scales must be finite and > 0");
+    } else if (q_dtype != kv_dtype) {
+        return fail(PA_ERR_UNSUPPORTED, "decode: q dtype must equal the cache dtype (fp8 caches excepted)");
+    }
+    if (tc && kv_dtype == PA_F32)
+        return fail(PA_ERR_UNSUPPORTED, "decode: f32 caches run on the CUDA-core path (pa_decode_simt)");
+    const void* kern = tc ? decode_kernel_tc(kv_dtype, q_dtype, D) : decode_kernel_simt(kv_dtype, q_dtype, D);
+    if (!kern) return fail(PA_ERR_UNSUPPORTED, "decode: no kernel for this dtype / head_dim combination");
+    const void* rkern = reduce_kernel(q_dtype, D);
+    if (!rkern) return fail(PA_ERR_UNSUPPORTED, "decode: no reduce kernel for this output dtype");
+    DeviceInfo dev;
+    if (!device_info(dev)) return fail(PA_ERR_CUDA, "decode: cannot query the current device");
+
+    const int G = Hq / Hkv;
+    const int e = dtype_bytes(kv_dtype);
+    const int eq = dtype_bytes(q_dtype);
+    const int MT = cdiv_h(G, 16);
+    if (MT > 8) return fail(PA_ERR_UNSUPPORTED, "decode: more than 128 query heads per KV head");
+    int HPC = 0;
+    for (int h = Hkv; h >= 1; --h) {
+        if (Hkv % h) continue;
+        if (h * MT > 8) continue;
+        if (16LL * h * D * e > 32 * 1024) continue;
+        HPC = h;
+        break;
+    }
+    if (HPC == 0) return fail(PA_ERR_UNSUPPORTED, "decode: no head grouping fits one CTA");
+    const int NHG = Hkv / HPC;
+    const int NCW = HPC * MT;
+    const int rpb = std::min(16, bs);
+    const int DH = D * e / 128;
+    if (DH < 1 || (D * e) % 128 != 0) return fail(PA_ERR_UNSUPPORTED, "decode: head_dim * elem bytes must be a multiple of 128");
+
+    DecodeParams p{};
+    p.out = out; p.q = q; p.block_tables = block_tables; p.seq_lens = seq_lens; p.err_flag = err_flag;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.D = D; p.bs = bs; p.NB = NB; p.MB = MB;
+    p.HPC = HPC; p.NHG = NHG; p.MT = MT; p.NCW = NCW;
+    p.P16 = partition_tokens / 16;
+    p.rpb = rpb;
+    p.box_bytes = static_cast<uint32_t>(rpb * HPC * DH * 128);
+    p.kv_bytes = static_cast<uint32_t>(16 * HPC * D * e);
+    p.q_bytes = static_cast<uint32_t>(HPC * G * D * eq);
+    const uint32_t q_slot = (p.q_bytes + 1023u) & ~1023u;
+    p.stage_bytes = 2 * p.kv_bytes + q_slot;
+    const uint32_t simtq = tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
+    const uint32_t extras = 2 * MAX_STAGES * 8 + MAX_STAGES * sizeof(StageDesc) + 32 * 8 + 64;
+    const long long budget = std::min(dev.max_smem, 227 * 1024) - 1024 - static_cast<long long>(simtq) - extras;
+    int stages = static_cast<int>(std::min<long long>(MAX_STAGES, budget / p.stage_bytes));
+    // keep roughly 160 KB of K/V in flight per CTA; more stages buy nothing
+    stages = std::min(stages, std::max(2, static_cast<int>((160 * 1024) / p.stage_bytes)));
+    if (stages < 2) return fail(PA_ERR_UNSUPPORTED, "decode: pipeline stages do not fit in shared memory");
+    p.stages = stages;
+    p.simtq_off = stages * p.stage_bytes;
+    p.bar_off = (p.simtq_off + simtq + 15u) & ~15u;
+    const size_t smem = 1024 + p.bar_off + extras;
+    const float log2e = 1.4426950408889634f;
+    p.qk_scale = scale * log2e * (kv_dtype == PA_FP8_E4M3 ? k_scale : 1.f);
+    p.v_scale = kv_dtype == PA_FP8_E4M3 ? v_scale : 1.f;
+
+    // workspace
+    const size_t need = workspace_bytes_for(B, Hq, D, MB * bs, partition_tokens, dev.sms);
+    if (!workspace) return fail(PA_ERR_WORKSPACE, "decode: workspace pointer is null");
+    if (workspace_bytes < need) return fail(PA_ERR_WORKSPACE, "decode: workspace smaller than pa_decode_workspace_size()");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PA_ERR_WORKSPACE, "decode: workspace must be 256-byte aligned");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.seq_info = reinterpret_cast<int2*>(ws); ws += align256(sizeof(int2) * static_cast<size_t>(B));
+    p.totals = reinterpret_cast<int*>(ws); ws += 256;
+    p.max_slots = max_slots_for(B, MB * bs, partition_tokens, dev.sms);
+    p.part_ml = reinterpret_cast<float2*>(ws); ws += align256(sizeof(float2) * static_cast<size_t>(p.max_slots) * Hq);
+    p.part_acc = reinterpret_cast<float*>(ws);
+
+    // tensor maps
+    alignas(64) CUtensorMap tk, tv;
+    p.per_head_copies = 0;
+    CUresult r1 = encode_kv_map(&tk, k_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, false);
+    CUresult r2 = r1 == CUDA_SUCCESS ? encode_kv_map(&tv, v_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, false) : r1;
+    if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
+        p.per_head_copies = 1;
+        r1 = encode_kv_map(&tk, k_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, true);
+        r2 = r1 == CUDA_SUCCESS ? encode_kv_map(&tv, v_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, true) : r1;
+        if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
+            char msg[96];
+            std::snprintf(msg, sizeof msg, "decode: cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r1 ? r1 : r2));
+            return fail(PA_ERR_CUDA, msg);
+        }
+    }
+
+    // grid: persistent CTAs, as many as fit, split into ranges x head groups
+    const int threads = (NCW + 1) * 32;
+    cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (ce != cudaSuccess) return fail_cuda("decode: set shared memory size", ce);
+    int per_sm = 0;
+    ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (ce != cudaSuccess) return fail_cuda("decode: occupancy query", ce);
+    per_sm = std::max(1, per_sm);
+    const long long chunk_bound = static_cast<long long>(B) * cdiv_h(static_cast<long long>(MB) * bs, 16);
+    long long NR = std::max(1LL, static_cast<long long>(per_sm) * dev.sms / NHG);
+    NR = std::min(NR, 2LL * dev.sms);
+    NR = std::min(NR, chunk_bound);
+    p.NR = static_cast<int>(NR);
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(NR * NHG));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    void* args[] = {&p, &tk, &tv};
+    ce = cudaLaunchKernelExC(&cfg, kern, args);
+    if (ce != cudaSuccess) return fail_cuda("decode: main kernel launch", ce);
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t rcfg{};
+    rcfg.gridDim = dim3(static_cast<unsigned>(B));
+    rcfg.blockDim = dim3(256);
+    rcfg.dynamicSmemBytes = 0;
+    rcfg.stream = stream;
+    rcfg.attrs = attr;
+    rcfg.numAttrs = 1;
+    void* rargs[] = {&p};
+    ce = cudaLaunchKernelExC(&rcfg, rkern, rargs);
+    if (ce != cudaSuccess) return fail_cuda("decode: reduce kernel launch", ce);
+    return PA_OK;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" const char* pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+extern "C" const char* pa_last_error_detail(void) { return g_detail; }
+
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
+                                           int partition_tokens) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 || partition_tokens < 0)
+        return 0;
+    DeviceInfo dev;
+    if (!device_info(dev)) return 0;
+    return workspace_bytes_for(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens, dev.sms);
+}
+
+extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
+                               const void* v_cache, pa_dtype kv_dtype, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, float scale, float k_scale, float v_scale,
+                               int partition_tokens, void* workspace, size_t workspace_bytes,
+                               int32_t* err_flag, cudaStream_t stream) {
+    return decode_impl(true, out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, max_blocks_per_seq,
+                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                       k_scale, v_scale, partition_tokens, workspace, workspace_bytes, err_flag, stream);
+}
+
+extern "C" pa_status pa_decode_simt(void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
+                                    const void* v_cache, pa_dtype kv_dtype, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, float scale, float k_scale, float v_scale,
+                                    int partition_tokens, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_flag, cudaStream_t stream) {
+    return decode_impl(false, out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, max_blocks_per_seq,
+                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                       k_scale, v_scale, partition_tokens, workspace, workspace_bytes, err_flag, stream);
+}

@@ -1,0 +1,870 @@
+// pa_decode_kernel.cuh -- paged decode attention: device code.
+//
+// What is computed (for every sequence i and query head h, g = h / G):
+//   s_t = scale * <q_h, K_t>, p = softmax(s), out_h = sum_t p_t V_t, t < L_i,
+// with K_t / V_t read through the block table ("vLLM intro part 2",
+// section 4; the PagedAttention note's three kernel steps: look up the block
+// table, load block by block, merge across blocks with online softmax).
+//
+// How (GB300 design):
+//  * Work unit = a 16-token chunk of one sequence for HPC KV heads.  The
+//    chunks of all sequences form one stream that is cut into NR equal
+//    ranges, one per persistent CTA (times NHG head groups), so every CTA
+//    moves the same number of bytes whatever the length mix.
+//  * One producer warp per CTA walks its range, prefetches block-table
+//    entries 32 at a time into registers, and issues TMA tile loads of the
+//    K and V rows of each chunk (all HPC heads of a block in one copy, 128-B
+//    swizzled in shared memory) plus a bulk copy of the query rows at each
+//    segment start, into a ring of stages guarded by full/empty mbarriers.
+//  * Consumer warps, one per (KV head, 16-row query tile), keep the GQA
+//    group's query heads packed as the M dimension of mma.sync m16n8k16
+//    (tensor-core variant) or as register rows (CUDA-core variant) and run
+//    online softmax over the chunk in fp32 (log2 domain).
+//  * A segment (the part of one sequence -- or of one partition of it --
+//    inside one CTA's range) ends by writing the final output directly when
+//    it covers the whole sequence, else an unnormalised partial
+//    (acc, m, l) for the log-sum-exp reduce kernel.
+// Every wait on an mbarrier is bounded in time; a timeout sets
+// PA_ERRBIT_WAIT_TIMEOUT and the CTA drains its outstanding copies and exits.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int CHUNK = 16;            // tokens per pipeline stage
+constexpr int MAX_STAGES = 8;
+constexpr int MAX_WARPS = 9;         // up to 8 consumers + 1 producer
+
+enum : uint32_t { SEG_START = 1u, SEG_END = 2u, DIRECT = 4u };
+
+struct StageDesc {
+    int seq;
+    int tok0;
+    int slot;
+    uint32_t vmask;
+    uint32_t flags;
+    int pad[3];
+};
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    float* part_acc;          // [max_slots][Hq][D]
+    float2* part_ml;          // [max_slots][Hq]  (m in log2 units, l)
+    int2* seq_info;           // [B] (first chunk, first unit)
+    int* totals;              // [0] chunks, [1] units
+    int32_t* err_flag;
+    int B, Hq, Hkv, G, D, bs, NB, MB;
+    int HPC, NHG, NR, MT, NCW;
+    int P16;                  // partition length in chunks, 0 = none
+    int max_slots;
+    float qk_scale;           // scale * log2(e) (* k_scale for fp8)
+    float v_scale;            // v_scale for fp8, else 1
+    int stages;
+    int rpb;                  // rows per TMA box = min(16, bs)
+    uint32_t box_bytes;       // bytes of one K (or V) box
+    uint32_t kv_bytes;        // bytes of one stage's K (or V) buffer
+    uint32_t q_bytes;         // query bytes copied per segment start
+    uint32_t stage_bytes;     // K + V + Q slot
+    uint32_t simtq_off;       // offset of the CUDA-core private query rows
+    uint32_t bar_off;         // offset of the barriers
+    int per_head_copies;      // 1: one TMA copy per (head, 128-B column block)
+};
+
+__device__ __forceinline__ int cdiv_i(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int clamp_len(int L, int maxL) {
+    return L < 0 ? 0 : (L > maxL ? maxL : L);
+}
+__device__ __forceinline__ int n_units(int L, int P16) {
+    const int n16 = cdiv_i(L, CHUNK);
+    return n16 == 0 ? 0 : (P16 > 0 ? cdiv_i(n16, P16) : 1);
+}
+// The range (CTA column) owning global chunk c: largest r with
+// floor(r * C / NR) <= c.
+__device__ __forceinline__ int range_of(int c, int C, int NR) {
+    return static_cast<int>(((static_cast<long long>(c) + 1) * NR - 1) / C);
+}
+// Range r covers chunks [floor(r*C/NR), floor((r+1)*C/NR)); with more
+// ranges than chunks some are empty and write no partial.
+__device__ __forceinline__ bool range_empty(int r, int C, int NR) {
+    return static_cast<long long>(r) * C / NR == (static_cast<long long>(r) + 1) * C / NR;
+}
+
+// ---------------------------------------------------------------------------
+// CTA prologue: chunk totals, this CTA's range, and the sequence holding
+// the range's first chunk.  CTA 0 also publishes per-sequence prefixes for
+// the reduce kernel.
+// ---------------------------------------------------------------------------
+struct Plan {
+    int cs, ce;               // chunk range [cs, ce)
+    int seq, S, U;            // first sequence, its first chunk and unit
+    int C, Ut;                // totals
+};
+
+__device__ __forceinline__ void warp_scan_pair(int& a, int& b) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, a, o);
+        const int y = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) { a += x; b += y; }
+    }
+}
+
+__device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch, int4* s_first, int2* s_tot,
+                          Plan& plan) {
+    const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = nth >> 5;
+    const int maxL = p.MB * p.bs;
+    const int per = cdiv_i(p.B, nth);
+    const int i0 = min(p.B, tid * per), i1 = min(p.B, i0 + per);
+    int csum = 0, usum = 0;
+    bool bad = false;
+    for (int i = i0; i < i1; ++i) {
+        const int Lraw = p.seq_lens[i];
+        bad |= (Lraw < 0 || Lraw > maxL);
+        const int L = clamp_len(Lraw, maxL);
+        csum += cdiv_i(L, CHUNK);
+        usum += n_units(L, p.P16);
+    }
+    if (bad && blockIdx.x == 0) raise_flag(p.err_flag, PA_ERRBIT_SEQ_TOO_LONG);
+    int ci = csum, ui = usum;           // inclusive within the warp
+    warp_scan_pair(ci, ui);
+    if (lane == 31) scratch[warp] = make_int2(ci, ui);
+    if (tid == 0) *s_first = make_int4(-1, 0, 0, 0);
+    __syncthreads();
+    if (warp == 0) {
+        int2 v = lane < nwarps ? scratch[lane] : make_int2(0, 0);
+        int a = v.x, b = v.y;
+        warp_scan_pair(a, b);
+        if (lane < nwarps) scratch[lane] = make_int2(a - v.x, b - v.y);   // exclusive
+        if (lane == nwarps - 1) *s_tot = make_int2(a, b);
+    }
+    __syncthreads();
+    const int2 wpre = scratch[warp];
+    const int cpre = wpre.x + ci - csum, upre = wpre.y + ui - usum;       // exclusive per thread
+    const int C = s_tot->x, Ut = s_tot->y;
+    const int cs = static_cast<int>(static_cast<long long>(range) * C / p.NR);
+    const int ce = static_cast<int>(static_cast<long long>(range + 1) * C / p.NR);
+    if (cs < ce && cpre <= cs && cs < cpre + csum) {
+        int S = cpre, U = upre;
+        for (int i = i0; i < i1; ++i) {
+            const int L = clamp_len(p.seq_lens[i], maxL);
+            const int n16 = cdiv_i(L, CHUNK);
+            if (cs < S + n16) { *s_first = make_int4(i, S, U, 0); break; }
+            S += n16;
+            U += n_units(L, p.P16);
+        }
+    }
+    if (blockIdx.x == 0) {
+        int S = cpre, U = upre;
+        for (int i = i0; i < i1; ++i) {
+            p.seq_info[i] = make_int2(S, U);
+            const int L = clamp_len(p.seq_lens[i], maxL);
+            S += cdiv_i(L, CHUNK);
+            U += n_units(L, p.P16);
+        }
+        if (tid == 0) { p.totals[0] = C; p.totals[1] = Ut; }
+    }
+    __syncthreads();
+    const int4 f = *s_first;
+    plan.cs = cs; plan.ce = ce; plan.seq = f.x; plan.S = f.y; plan.U = f.z;
+    plan.C = C; plan.Ut = Ut;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addressing of one stage's K or V buffer.  A box holds
+// `rpb` token rows of all HPC heads, laid out [col_block][head][row][128 B]
+// with the 128-B TMA swizzle; a 16-token chunk is 16 / rpb boxes.
+// ---------------------------------------------------------------------------
+struct KVLayout {
+    uint32_t box_bytes, head_stride, dh_stride;
+    int rpb;
+    __device__ __forceinline__ uint32_t row_base(int tok, int hl) const {
+        const int b = tok / rpb, r = tok - b * rpb;
+        return b * box_bytes + (hl * rpb + r) * 128u;
+    }
+    // byte offset of 16-byte column chunk `c` (c = 0 .. D*e/16-1) of token row
+    __device__ __forceinline__ uint32_t chunk_addr(uint32_t rowbase, int tok, int c) const {
+        return rowbase + (c >> 3) * dh_stride + (((c & 7) ^ (tok & 7)) << 4);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <class KV, class QT, int D, bool TC>
+struct DecodeKernel {
+    using KT = typename KV::T;
+    using QE = typename QT::T;
+    static constexpr bool FP8 = (KV::code == PA_FP8_E4M3);
+    static constexpr bool MMA_BF16 = (KV::code == PA_BF16);   // fp8 runs in f16
+    static constexpr int NT = D / 8;          // 8-wide output column tiles
+    static constexpr int KS = D / 16;         // 16-deep k-steps over head_dim
+    static constexpr int ROWB = D * KV::bytes;  // bytes of one K/V row
+    static constexpr int CPR = ROWB / 16;     // 16-byte chunks per row
+
+    // ---------------- producer ----------------
+    static __device__ void producer(const DecodeParams& p, const Plan& pl, int hg, uint8_t* base,
+                                    uint64_t* full, uint64_t* empty, StageDesc* descs,
+                                    const CUtensorMap* tk, const CUtensorMap* tv) {
+        const int lane = threadIdx.x & 31;
+        const int S = p.stages;
+        const int maxL = p.MB * p.bs;
+        int i = pl.seq, Si = pl.S, Ui = pl.U;
+        int L = clamp_len(p.seq_lens[i], maxL);
+        int n16 = cdiv_i(L, CHUNK), nbl = cdiv_i(L, p.bs);
+        int j = pl.cs - Si;
+        int wbase = INT_MIN / 2, wval = -1;
+        const int nb = p.bs >= CHUNK ? 1 : CHUNK / p.bs;      // boxes per chunk
+        const int hq0 = hg * p.HPC * p.G;
+        int issued = 0;
+        bool ok = true;
+        for (int k = pl.cs; k < pl.ce; ++k) {
+            while (j >= n16) {
+                Si += n16; Ui += n_units(L, p.P16); ++i;
+                L = clamp_len(p.seq_lens[i], maxL);
+                n16 = cdiv_i(L, CHUNK); nbl = cdiv_i(L, p.bs); j = 0; wbase = INT_MIN / 2;
+            }
+            const int tok0 = j * CHUNK;
+            const int b0 = tok0 / p.bs;
+            if (b0 < wbase || b0 + nb - 1 >= wbase + 32) {
+                wbase = b0;
+                const int idx = wbase + lane;
+                wval = idx < nbl ? __ldg(p.block_tables + static_cast<size_t>(i) * p.MB + idx) : -1;
+            }
+            int blk[2];
+            blk[0] = __shfl_sync(0xffffffffu, wval, b0 - wbase);
+            blk[1] = __shfl_sync(0xffffffffu, wval, min(b0 + 1 - wbase, 31));
+            if (lane == 0) {
+                const int slot = issued % S;
+                const uint32_t round = issued / S;
+                if (issued >= S && !mbar_wait_bounded(&empty[slot], (round - 1) & 1u)) {
+                    raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                    ok = false;
+                }
+                if (ok) {
+                    const int ntok = min(CHUNK, L - tok0);
+                    uint32_t vmask = (ntok >= 32) ? 0xffffffffu : ((1u << ntok) - 1u);
+                    vmask &= 0xffffu;
+                    uint32_t nbox_issued = 0;
+                    uint8_t* kbuf = base + slot * p.stage_bytes;
+                    uint8_t* vbuf = kbuf + p.kv_bytes;
+                    uint32_t issue_mask = 0;
+                    for (int b = 0; b < nb; ++b) {
+                        const int first = b * p.rpb;
+                        if (first >= ntok) continue;                 // nothing valid here
+                        const int id = blk[b];
+                        const uint32_t rows = ((1u << p.rpb) - 1u) << first;
+                        if (id < 0 || id >= p.NB) {
+                            raise_flag(p.err_flag, PA_ERRBIT_BAD_BLOCK);
+                            vmask &= ~rows;
+                            continue;
+                        }
+                        issue_mask |= 1u << b;
+                        ++nbox_issued;
+                    }
+                    uint32_t flags = 0;
+                    const bool seg_start = (k == pl.cs) || (j == 0) || (p.P16 > 0 && j % p.P16 == 0);
+                    const bool seg_end = (k == pl.ce - 1) || (j == n16 - 1) ||
+                                         (p.P16 > 0 && (j + 1) % p.P16 == 0);
+                    if (seg_start) flags |= SEG_START;
+                    if (seg_end) flags |= SEG_END;
+                    const int nu = n_units(L, p.P16);
+                    if (nu == 1 && Si >= pl.cs && Si + n16 <= pl.ce) flags |= DIRECT;
+                    StageDesc d;
+                    d.seq = i; d.tok0 = tok0; d.vmask = vmask; d.flags = flags;
+                    d.slot = (blockIdx.x / p.NHG) + Ui + (p.P16 > 0 ? j / p.P16 : 0);
+                    descs[slot] = d;
+                    const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (seg_start ? p.q_bytes : 0u);
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    for (int b = 0; b < nb; ++b) {
+                        if (!((issue_mask >> b) & 1u)) continue;
+                        const int row0 = blk[b] * p.bs + (p.bs > CHUNK ? (tok0 % p.bs) : 0);
+                        uint8_t* kd = kbuf + b * p.box_bytes;
+                        uint8_t* vd = vbuf + b * p.box_bytes;
+                        if (!p.per_head_copies) {
+                            tma_load_4d(kd, tk, &full[slot], 0, row0, hg * p.HPC, 0);
+                            tma_load_4d(vd, tv, &full[slot], 0, row0, hg * p.HPC, 0);
+                        } else {
+                            const int DH = ROWB / 128;
+                            const int E128 = 128 / KV::bytes;
+                            for (int dh = 0; dh < DH; ++dh)
+                                for (int hl = 0; hl < p.HPC; ++hl) {
+                                    const uint32_t off = ((dh * p.HPC + hl) * p.rpb) * 128u;
+                                    tma_load_3d(kd + off, tk, &full[slot], dh * E128, hg * p.HPC + hl, row0);
+                                    tma_load_3d(vd + off, tv, &full[slot], dh * E128, hg * p.HPC + hl, row0);
+                                }
+                        }
+                    }
+                    if (seg_start) {
+                        const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
+                            (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
+                        bulk_load(kbuf + 2 * p.kv_bytes, qsrc, p.q_bytes, &full[slot]);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ++issued;
+            ++j;
+        }
+        // drain: every copy this CTA issued must land before the CTA exits
+        if (lane == 0) {
+            const int first = max(0, issued - S);
+            for (int st = first; st < issued; ++st) {
+                if (!mbar_wait_bounded(&full[st % S], (st / S) & 1u)) {
+                    raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    }
+
+    // ---------------- output of a finished segment ----------------
+    template <typename OutT>
+    static __device__ __forceinline__ void store_pair(OutT* dst, float a, float b) {
+        dst[0] = from_float<OutT>(a);
+        dst[1] = from_float<OutT>(b);
+    }
+
+    // Column of accumulator element (tile nt, column pair index within the
+    // tile n) in head_dim coordinates.
+    static __device__ __forceinline__ int out_col(int nt, int n) {
+        if constexpr (FP8) {
+            return 16 * (nt >> 1) + 2 * n + (nt & 1);
+        } else {
+            return nt * 8 + n;
+        }
+    }
+
+    // ---------------- tensor-core consumer ----------------
+    static __device__ void consumer_tc(const DecodeParams& p, const Plan& pl, int hg, int w,
+                                       uint8_t* base, uint64_t* full, uint64_t* empty,
+                                       const StageDesc* descs) {
+        const int lane = threadIdx.x & 31;
+        const int g4 = lane >> 2, t4 = lane & 3;
+        const int hl = w / p.MT, mt = w - hl * p.MT;
+        const int rows_valid = min(16, p.G - 16 * mt);
+        const int S = p.stages;
+        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
+                           static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
+        // per-lane ldmatrix rows
+        const int mi = lane >> 3, r8 = lane & 7;
+        const int tokK = (mi >> 1) * 8 + r8;       // K (non-transposed) row
+        const int tokV = (mi & 1) * 8 + r8;        // V (transposed) row
+        const uint32_t rbK = lay.row_base(tokK, hl), rbV = lay.row_base(tokV, hl);
+
+        float acc[NT][4];
+        uint32_t qa[KS][4];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const int qrow_lo = hl * p.G + 16 * mt;     // first local query row of this tile
+        const int out_h0 = hg * p.HPC * p.G + qrow_lo;
+
+        for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
+            const int slot = st % S;
+            if (!mbar_wait_bounded(&full[slot], (st / S) & 1u)) {
+                if (lane == 0) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                return;
+            }
+            const StageDesc d = descs[slot];
+            uint8_t* kbuf = base + slot * p.stage_bytes;
+            uint8_t* vbuf = kbuf + p.kv_bytes;
+            const uint8_t* qbuf = kbuf + 2 * p.kv_bytes;
+            if (d.flags & SEG_START) {
+                load_q_frags(qa, qbuf, qrow_lo, rows_valid, lane);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+                m0 = m1 = -INFINITY; l0 = l1 = 0.f;
+            }
+            bool wrote = false;
+            if (d.vmask != 0xffffu) {     // zero masked V rows of this head (pool garbage may be NaN)
+                for (int idx = lane; idx < CHUNK * CPR; idx += 32) {
+                    const int tok = idx / CPR, c = idx - tok * CPR;
+                    if (!((d.vmask >> tok) & 1u)) {
+                        const uint32_t a = lay.chunk_addr(lay.row_base(tok, hl), tok, c);
+                        *reinterpret_cast<uint4*>(vbuf + a) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                wrote = true;
+                __syncwarp();
+            }
+            // ---- S = Q K^T (16 rows x 16 tokens) ----
+            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const uint32_t kb = smem_u32(kbuf);
+            if constexpr (!FP8) {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + lay.chunk_addr(rbK, tokK, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+                    mma_16816<MMA_BF16>(s[0], qa[ks], b0, b1);
+                    mma_16816<MMA_BF16>(s[1], qa[ks], b2, b3);
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KS; ks += 2) {
+                    uint32_t r0, r1, r2, r3;    // (tile0,ks) (tile0,ks+1) (tile1,ks) (tile1,ks+1)
+                    ldsm_x4(kb + lay.chunk_addr(rbK, tokK, ks + (mi & 1)), r0, r1, r2, r3);
+                    mma_16816<false>(s[0], qa[ks], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
+                    mma_16816<false>(s[0], qa[ks + 1], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+                    mma_16816<false>(s[1], qa[ks], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
+                    mma_16816<false>(s[1], qa[ks + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+                }
+            }
+            // ---- online softmax (log2 domain), rows g4 and g4+8 ----
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = nt * 8 + 2 * t4 + (e & 1);
+                    s[nt][e] = ((d.vmask >> col) & 1u) ? s[nt][e] * p.qk_scale : -INFINITY;
+                }
+            float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+            float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+            m0 = mn0; m1 = mn1;
+            float pr[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                pr[nt][0] = exp2f(s[nt][0] - mu0);
+                pr[nt][1] = exp2f(s[nt][1] - mu0);
+                pr[nt][2] = exp2f(s[nt][2] - mu1);
+                pr[nt][3] = exp2f(s[nt][3] - mu1);
+            }
+            l0 = l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+            l1 = l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+            if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    acc[nt][0] *= al0; acc[nt][1] *= al0;
+                    acc[nt][2] *= al1; acc[nt][3] *= al1;
+                }
+            }
+            uint32_t pa[4];
+            pa[0] = pack2(pr[0][0], pr[0][1], MMA_BF16);
+            pa[1] = pack2(pr[0][2], pr[0][3], MMA_BF16);
+            pa[2] = pack2(pr[1][0], pr[1][1], MMA_BF16);
+            pa[3] = pack2(pr[1][2], pr[1][3], MMA_BF16);
+            // ---- acc += P V ----
+            const uint32_t vb = smem_u32(vbuf);
+            if constexpr (!FP8) {
+#pragma unroll
+                for (int j2 = 0; j2 < NT / 2; ++j2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, 2 * j2 + (mi >> 1)), b0, b1, b2, b3);
+                    mma_16816<MMA_BF16>(acc[2 * j2], pa, b0, b1);
+                    mma_16816<MMA_BF16>(acc[2 * j2 + 1], pa, b2, b3);
+                }
+            } else {
+#pragma unroll
+                for (int c2 = 0; c2 < D / 16; c2 += 2) {
+                    uint32_t r0, r1, r2, r3;  // (tok0-7,c) (tok8-15,c) (tok0-7,c+1) (tok8-15,c+1)
+                    ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, c2 + (mi >> 1)), r0, r1, r2, r3);
+                    const uint32_t x0 = __byte_perm(r0, 0, 0x3120), x1 = __byte_perm(r1, 0, 0x3120);
+                    const uint32_t x2 = __byte_perm(r2, 0, 0x3120), x3 = __byte_perm(r3, 0, 0x3120);
+                    mma_16816<false>(acc[2 * c2], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
+                    mma_16816<false>(acc[2 * c2 + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
+                    mma_16816<false>(acc[2 * c2 + 2], pa, e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x3));
+                    mma_16816<false>(acc[2 * c2 + 3], pa, e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16));
+                }
+            }
+            if (d.flags & SEG_END) {
+                float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+                lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+                float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+                lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+                const bool v0 = g4 < rows_valid, v1 = g4 + 8 < rows_valid;
+                if (d.flags & DIRECT) {
+                    QE* o = static_cast<QE*>(p.out) + static_cast<size_t>(d.seq) * p.Hq * D;
+                    const float i0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
+                    const float i1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int c0 = out_col(nt, 2 * t4), c1 = out_col(nt, 2 * t4 + 1);
+                        if (v0) {
+                            QE* r = o + static_cast<size_t>(out_h0 + g4) * D;
+                            r[c0] = from_float<QE>(acc[nt][0] * i0);
+                            r[c1] = from_float<QE>(acc[nt][1] * i0);
+                        }
+                        if (v1) {
+                            QE* r = o + static_cast<size_t>(out_h0 + g4 + 8) * D;
+                            r[c0] = from_float<QE>(acc[nt][2] * i1);
+                            r[c1] = from_float<QE>(acc[nt][3] * i1);
+                        }
+                    }
+                } else if (d.slot < p.max_slots) {
+                    float* pa_ = p.part_acc + static_cast<size_t>(d.slot) * p.Hq * D;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int c0 = out_col(nt, 2 * t4), c1 = out_col(nt, 2 * t4 + 1);
+                        if (v0) {
+                            float* r = pa_ + static_cast<size_t>(out_h0 + g4) * D;
+                            r[c0] = acc[nt][0] * p.v_scale;
+                            r[c1] = acc[nt][1] * p.v_scale;
+                        }
+                        if (v1) {
+                            float* r = pa_ + static_cast<size_t>(out_h0 + g4 + 8) * D;
+                            r[c0] = acc[nt][2] * p.v_scale;
+                            r[c1] = acc[nt][3] * p.v_scale;
+                        }
+                    }
+                    if (t4 == 0) {
+                        float2* ml = p.part_ml + static_cast<size_t>(d.slot) * p.Hq;
+                        if (v0) ml[out_h0 + g4] = make_float2(m0, lt0);
+                        if (v1) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
+                    }
+                }
+            }
+            if (wrote) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+    }
+
+    // A fragments of this tile's query rows (16 x D) from the stage's query
+    // copy; rows past the group are zero.
+    static __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[KS][4], const uint8_t* qbuf,
+                                                        int qrow_lo, int rows_valid, int lane) {
+        const int g4 = lane >> 2, t4 = lane & 3;
+        if constexpr (!FP8) {
+            const int mi = lane >> 3, r8 = lane & 7;
+            int row = (mi & 1) * 8 + r8;
+            if (row >= rows_valid) row = 0;
+            const uint32_t rb = smem_u32(qbuf) + static_cast<uint32_t>((qrow_lo + row) * D * 2);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                ldsm_x4(rb + (2 * ks + (mi >> 1)) * 16, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+            }
+        } else {
+            // head_dim order inside a 16-wide k-step is permuted to match the
+            // byte order of e4m3 key rows: logical k (2t, 2t+1, 2t+8, 2t+9)
+            // holds physical dims (4t, 4t+1, 4t+2, 4t+3).
+            const QE* q0 = reinterpret_cast<const QE*>(qbuf) + static_cast<size_t>(qrow_lo + min(g4, rows_valid - 1)) * D;
+            const QE* q1 = reinterpret_cast<const QE*>(qbuf) + static_cast<size_t>(qrow_lo + min(g4 + 8, rows_valid - 1)) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int d0 = 16 * ks + 4 * t4;
+                qa[ks][0] = pack2(to_float(q0[d0]), to_float(q0[d0 + 1]), false);
+                qa[ks][1] = pack2(to_float(q1[d0]), to_float(q1[d0 + 1]), false);
+                qa[ks][2] = pack2(to_float(q0[d0 + 2]), to_float(q0[d0 + 3]), false);
+                qa[ks][3] = pack2(to_float(q1[d0 + 2]), to_float(q1[d0 + 3]), false);
+            }
+        }
+        if (g4 >= rows_valid) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) { qa[ks][0] = 0u; qa[ks][2] = 0u; }
+        }
+        if (g4 + 8 >= rows_valid) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) { qa[ks][1] = 0u; qa[ks][3] = 0u; }
+        }
+    }
+
+    // ---------------- CUDA-core consumer ----------------
+    // Lanes (t, half) = (lane & 15, lane >> 4) compute the dot products of
+    // token t over half of head_dim for up to 16 query rows; for P*V each
+    // lane owns D/32 consecutive columns.
+    static __device__ void consumer_simt(const DecodeParams& p, const Plan& pl, int hg, int w,
+                                         uint8_t* base, uint64_t* full, uint64_t* empty,
+                                         const StageDesc* descs, float* qpriv) {
+        constexpr int R = 16;
+        constexpr int VE = 16 / KV::bytes;     // elements per 16-byte chunk
+        constexpr int DPL = D / 32;            // columns per lane in P*V
+        const int lane = threadIdx.x & 31;
+        const int tq = lane & 15, half = lane >> 4;
+        const int hl = w / p.MT, mt = w - hl * p.MT;
+        const int nr = min(R, p.G - 16 * mt);
+        const int S = p.stages;
+        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
+                           static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
+        const int qrow_lo = hl * p.G + 16 * mt;
+        const int out_h0 = hg * p.HPC * p.G + qrow_lo;
+        float* qp = qpriv + static_cast<size_t>(w) * R * D;   // this warp's query rows, fp32
+
+        float acc[R][DPL];
+        float m[R], l[R];
+        for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
+            const int slot = st % S;
+            if (!mbar_wait_bounded(&full[slot], (st / S) & 1u)) {
+                if (lane == 0) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                return;
+            }
+            const StageDesc d = descs[slot];
+            const uint8_t* kbuf = base + slot * p.stage_bytes;
+            const uint8_t* vbuf = kbuf + p.kv_bytes;
+            const QE* qbuf = reinterpret_cast<const QE*>(kbuf + 2 * p.kv_bytes);
+            if (d.flags & SEG_START) {
+                for (int e = lane; e < nr * D; e += 32)
+                    qp[e] = to_float(qbuf[static_cast<size_t>(qrow_lo) * D + e]);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    m[r] = -INFINITY; l[r] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) acc[r][c] = 0.f;
+                }
+                __syncwarp();
+            }
+            // ---- scores of token tq over half of head_dim ----
+            float s[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) s[r] = 0.f;
+            const uint32_t rbk = lay.row_base(tq, hl);
+#pragma unroll 2
+            for (int c = half * (CPR / 2); c < (half + 1) * (CPR / 2); ++c) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(kbuf + lay.chunk_addr(rbk, tq, c));
+                float kf[VE];
+                unpack16<KV>(raw, kf);
+                const int d0 = c * VE;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r < nr) {
+                        const float* qr = qp + r * D + d0;
+                        float a = s[r];
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) a = fmaf(qr[e], kf[e], a);
+                        s[r] = a;
+                    }
+                }
+            }
+            const bool valid = (d.vmask >> tq) & 1u;
+            float p_[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (r < nr) {
+                    float x = s[r] + __shfl_xor_sync(0xffffffffu, s[r], 16);
+                    x = valid ? x * p.qk_scale : -INFINITY;
+                    float cm = x;
+                    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+                    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+                    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+                    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+                    const float mn = fmaxf(m[r], cm);
+                    const float mu = (mn == -INFINITY) ? 0.f : mn;
+                    const float al = exp2f(m[r] - mu);
+                    m[r] = mn;
+                    const float pv = exp2f(x - mu);
+                    float cs = pv;
+                    cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+                    cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+                    cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+                    cs += __shfl_xor_sync(0xffffffffu, cs, 8);
+                    l[r] = l[r] * al + cs;
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) acc[r][c] *= al;
+                    p_[r] = pv;
+                }
+            }
+            // ---- acc += p V over the chunk's valid tokens ----
+            const int cidx = (lane * DPL * KV::bytes) / 16;           // 16-byte chunk holding my columns
+            const int cbyte = (lane * DPL * KV::bytes) % 16;
+            for (int t = 0; t < CHUNK; ++t) {
+                if (!((d.vmask >> t) & 1u)) continue;
+                const uint8_t* src = vbuf + lay.chunk_addr(lay.row_base(t, hl), t, cidx) + cbyte;
+                float vf[DPL];
+                load_cols<KV, DPL>(src, vf);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r < nr) {
+                        const float pt = __shfl_sync(0xffffffffu, p_[r], t);
+#pragma unroll
+                        for (int c = 0; c < DPL; ++c) acc[r][c] = fmaf(pt, vf[c], acc[r][c]);
+                    }
+                }
+            }
+            if (d.flags & SEG_END) {
+                const int c0 = lane * DPL;
+                if (d.flags & DIRECT) {
+                    QE* o = static_cast<QE*>(p.out) + static_cast<size_t>(d.seq) * p.Hq * D;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (r < nr) {
+                            const float inv = l[r] > 0.f ? p.v_scale / l[r] : 0.f;
+                            QE* row = o + static_cast<size_t>(out_h0 + r) * D + c0;
+#pragma unroll
+                            for (int c = 0; c < DPL; ++c) row[c] = from_float<QE>(acc[r][c] * inv);
+                        }
+                    }
+                } else if (d.slot < p.max_slots) {
+                    float* pa_ = p.part_acc + static_cast<size_t>(d.slot) * p.Hq * D;
+                    float2* ml = p.part_ml + static_cast<size_t>(d.slot) * p.Hq;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (r < nr) {
+                            float* row = pa_ + static_cast<size_t>(out_h0 + r) * D + c0;
+#pragma unroll
+                            for (int c = 0; c < DPL; ++c) row[c] = acc[r][c] * p.v_scale;
+                            if (lane == 0) ml[out_h0 + r] = make_float2(m[r], l[r]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+    }
+
+    template <class K2>
+    static __device__ __forceinline__ void unpack16(const uint4 raw, float (&f)[16 / K2::bytes]) {
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        if constexpr (K2::code == PA_F32) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = __uint_as_float(w[e]);
+        } else if constexpr (K2::code == PA_F16) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                f[2 * e] = x.x; f[2 * e + 1] = x.y;
+            }
+        } else if constexpr (K2::code == PA_BF16) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+                f[2 * e] = x.x; f[2 * e + 1] = x.y;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t h01 = e4m3x2_to_f16x2(w[e]), h23 = e4m3x2_to_f16x2(w[e] >> 16);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+                f[4 * e] = a.x; f[4 * e + 1] = a.y; f[4 * e + 2] = b.x; f[4 * e + 3] = b.y;
+            }
+        }
+    }
+
+    template <class K2, int N>
+    static __device__ __forceinline__ void load_cols(const uint8_t* src, float (&f)[N]) {
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+            if constexpr (K2::code == PA_F32) f[c] = reinterpret_cast<const float*>(src)[c];
+            else if constexpr (K2::code == PA_F16) f[c] = __half2float(reinterpret_cast<const __half*>(src)[c]);
+            else if constexpr (K2::code == PA_BF16) f[c] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[c]);
+            else f[c] = fp8_to_float(src[c]);
+        }
+    }
+};
+
+template <class KV, class QT, int D, bool TC>
+__global__ void __launch_bounds__(MAX_WARPS * 32, 1)
+pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv) {
+    using K = DecodeKernel<KV, QT, D, TC>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + p.bar_off);
+    uint64_t* empty = full + MAX_STAGES;
+    StageDesc* descs = reinterpret_cast<StageDesc*>(empty + MAX_STAGES);
+    int2* scratch = reinterpret_cast<int2*>(descs + MAX_STAGES);
+    int4* s_first = reinterpret_cast<int4*>(scratch + 32);
+    int2* s_tot = reinterpret_cast<int2*>(s_first + 1);
+
+    const int hg = blockIdx.x % p.NHG;
+    const int range = blockIdx.x / p.NHG;
+    Plan pl;
+    make_plan(p, range, scratch, s_first, s_tot, pl);
+    if (pl.cs >= pl.ce || pl.seq < 0) return;
+
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], p.NCW);
+        }
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (warp == p.NCW) {
+        if ((threadIdx.x & 31) == 0) { prefetch_tensormap(&tk); prefetch_tensormap(&tv); }
+        K::producer(p, pl, hg, base, full, empty, descs, &tk, &tv);
+    } else if (warp < p.NCW) {
+        if constexpr (TC) {
+            K::consumer_tc(p, pl, hg, warp, base, full, empty, descs);
+        } else {
+            K::consumer_simt(p, pl, hg, warp, base, full, empty, descs,
+                             reinterpret_cast<float*>(base + p.simtq_off));
+        }
+    }
+    grid_dependents_launch();
+}
+
+// ---------------------------------------------------------------------------
+// log-sum-exp merge of the partials of sequences split across CTAs or
+// partitions:  M = max m_k,  out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
+// One CTA per sequence, one warp per head at a time, lanes over head_dim.
+// ---------------------------------------------------------------------------
+template <typename OutT, int D>
+__global__ void __launch_bounds__(256)
+pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
+    grid_dependency_wait();
+    const int i = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int L = clamp_len(p.seq_lens[i], p.MB * p.bs);
+    OutT* out = static_cast<OutT*>(p.out) + static_cast<size_t>(i) * p.Hq * D;
+    constexpr int DPL = D / 32;
+    if (L == 0) {
+        for (int e = threadIdx.x; e < p.Hq * D; e += blockDim.x) out[e] = from_float<OutT>(0.f);
+        return;
+    }
+    const int2 info = p.seq_info[i];
+    const int C = p.totals[0];
+    const int n16 = cdiv_i(L, CHUNK), nu = n_units(L, p.P16);
+    if (nu == 1 && range_of(info.x, C, p.NR) == range_of(info.x + n16 - 1, C, p.NR)) return;
+    for (int h = warp; h < p.Hq; h += nw) {
+        // pass 1: the running maximum over every partial of (i, h)
+        float M = -INFINITY;
+        for (int u = 0; u < nu; ++u) {
+            const int a = info.x + (p.P16 > 0 ? u * p.P16 : 0);
+            const int b = p.P16 > 0 ? min(a + p.P16, info.x + n16) : info.x + n16;
+            const int r0 = range_of(a, C, p.NR), r1 = range_of(b - 1, C, p.NR);
+            for (int r = r0 + lane; r <= r1; r += 32) {
+                if (range_empty(r, C, p.NR)) continue;
+                const int slot = r + info.y + u;
+                if (slot < p.max_slots) M = fmaxf(M, p.part_ml[static_cast<size_t>(slot) * p.Hq + h].x);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float Mu = (M == -INFINITY) ? 0.f : M;
+        float num[DPL];
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) num[c] = 0.f;
+        float den = 0.f;
+        for (int u = 0; u < nu; ++u) {
+            const int a = info.x + (p.P16 > 0 ? u * p.P16 : 0);
+            const int b = p.P16 > 0 ? min(a + p.P16, info.x + n16) : info.x + n16;
+            const int r0 = range_of(a, C, p.NR), r1 = range_of(b - 1, C, p.NR);
+            for (int r = r0; r <= r1; ++r) {
+                if (range_empty(r, C, p.NR)) continue;
+                const int slot = r + info.y + u;
+                if (slot >= p.max_slots) continue;
+                const float2 ml = p.part_ml[static_cast<size_t>(slot) * p.Hq + h];
+                const float wgt = exp2f(ml.x - Mu);
+                den = fmaf(wgt, ml.y, den);
+                const float* src = p.part_acc + (static_cast<size_t>(slot) * p.Hq + h) * D + lane * DPL;
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) num[c] = fmaf(wgt, src[c], num[c]);
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        OutT* o = out + static_cast<size_t>(h) * D + lane * DPL;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) o[c] = from_float<OutT>(num[c] * inv);
+    }
+}
+
+}  // namespace pa

@@ -1,0 +1,36 @@
+// pa_decode_simt.cu -- CUDA-core (FMA) instantiations of the paged decode
+// kernel, and the log-sum-exp reduce kernel.
+#include <cuda.h>
+
+#include "pa_decode_kernel.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D) {
+#define PA_SIMT_CASE(KVT, QTT)                                                                  \
+    if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 128, false>); \
+    if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 64, false>);   \
+    return nullptr;
+    if (kv == PA_F32 && q == PA_F32) { PA_SIMT_CASE(F32T, F32T) }
+    if (kv == PA_F16 && q == PA_F16) { PA_SIMT_CASE(F16T, F16T) }
+    if (kv == PA_BF16 && q == PA_BF16) { PA_SIMT_CASE(BF16T, BF16T) }
+    if (kv == PA_FP8_E4M3 && q == PA_F16 && D == 128)
+        return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, false>);
+    if (kv == PA_FP8_E4M3 && q == PA_BF16 && D == 128)
+        return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, false>);
+#undef PA_SIMT_CASE
+    return nullptr;
+}
+
+const void* reduce_kernel(pa_dtype out, int D) {
+    if (out == PA_F32) return D == 128 ? reinterpret_cast<const void*>(&pa_reduce_kernel<float, 128>)
+                                       : reinterpret_cast<const void*>(&pa_reduce_kernel<float, 64>);
+    if (out == PA_F16) return D == 128 ? reinterpret_cast<const void*>(&pa_reduce_kernel<__half, 128>)
+                                       : reinterpret_cast<const void*>(&pa_reduce_kernel<__half, 64>);
+    if (out == PA_BF16) return D == 128 ? reinterpret_cast<const void*>(&pa_reduce_kernel<__nv_bfloat16, 128>)
+                                        : reinterpret_cast<const void*>(&pa_reduce_kernel<__nv_bfloat16, 64>);
+    return nullptr;
+}
+
+}  // namespace pa

@@ -1,0 +1,11 @@
+// pa_kernels.h -- lookup of the decode kernel instantiations (host side).
+#pragma once
+
+#include "../../include/pa.h"
+
+namespace pa {
+// Kernel entry for the given cache dtype, query dtype and head_dim, or null.
+const void* decode_kernel_tc(pa_dtype kv, pa_dtype q, int D);
+const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D);
+const void* reduce_kernel(pa_dtype out, int D);
+}  // namespace pa

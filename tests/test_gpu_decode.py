@@ -1,0 +1,248 @@
+"""GPU parity of paged decode attention against the oracle, through the
+C-ABI.  Small cases are compared element by element in full; the full-size
+workloads on sampled (sequence, head) outputs the oracle computes one by one
+plus bit-exact pools and properties that hold at any size."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_69_gb300 as pa
+from paged_kv_cache_69_gb300 import inputs
+
+from _harness import GpuStep, assert_caches_equal, compare, oracle_caches, oracle_problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pa.build()
+
+
+def _full_check(wl, simt=False, partition_tokens=0, check_pool=True):
+    ref_k, ref_v = oracle_caches(wl)
+    ref = oracle.decode(oracle_problem(wl, ref_k, ref_v))
+    step = GpuStep(wl)
+    out = step.run(simt=simt, partition_tokens=partition_tokens)
+    if check_pool:
+        assert_caches_equal(step, ref_k, ref_v)
+    assert step.err.item() == 0, f"device error flag {step.err.item()}"
+    return compare(out, ref, wl.kv_dtype, wl.name), step, ref
+
+
+def test_tiny_fp32_config():
+    """4 sequences {5,16,17,40}, GQA 2, head_dim 64, block 16, fp32."""
+    _full_check(inputs.tiny_fp32(), simt=True)
+
+
+CASES = [
+    # kv, q, D, bs, Hq, Hkv, lens
+    ("f16", None, 128, 16, 28, 4, [1, 15, 16, 17, 100, 333, 1000, 2049]),
+    ("bf16", None, 128, 16, 32, 8, [20, 40, 41, 300, 777]),
+    ("bf16", None, 128, 8, 32, 8, [1, 7, 8, 9, 23, 40, 129]),
+    ("f16", None, 64, 32, 16, 2, [3, 31, 32, 33, 500]),
+    ("bf16", None, 64, 16, 4, 4, [10, 64, 65]),            # MHA, G = 1
+    ("f16", None, 128, 16, 32, 1, [50, 260]),              # MQA, G = 32: two query tiles
+    ("f16", None, 128, 32, 64, 4, [70, 1030]),             # G = 16
+    ("fp8_e4m3", "bf16", 128, 32, 32, 8, [1, 31, 32, 33, 900]),
+    ("fp8_e4m3", "f16", 128, 16, 28, 4, [5, 16, 17, 400]),
+    ("f32", None, 128, 16, 8, 2, [3, 17, 90]),
+    ("f32", None, 64, 8, 6, 3, [1, 8, 9, 64]),
+]
+
+
+def _case(kv, qd, D, bs, Hq, Hkv, lens, seed=0):
+    return inputs.make_random(lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                              kv_dtype=kv, q_dtype=qd, spare_blocks=11, seed=seed,
+                              name=f"{kv}_D{D}_bs{bs}_{Hq}x{Hkv}")
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[1]}-D{c[2]}-bs{c[3]}-{c[4]}x{c[5]}")
+@pytest.mark.parametrize("variant", ["tc", "simt"])
+@pytest.mark.parametrize("partition_tokens", [0, 32])
+def test_decode_small(case, variant, partition_tokens):
+    kv = case[0]
+    if variant == "tc" and kv == "f32":
+        pytest.skip("f32 caches run on the CUDA-core path")
+    wl = _case(*case, seed=len(case[6]))
+    _full_check(wl, simt=(variant == "simt"), partition_tokens=partition_tokens)
+
+
+def test_one_long_sequence_spans_every_cta():
+    wl = _case("bf16", None, 128, 16, 8, 1, [40000], seed=3)
+    _full_check(wl)
+    _full_check(wl, partition_tokens=512)
+
+
+def test_many_short_sequences_direct_writes():
+    g = torch.Generator().manual_seed(4)
+    lens = torch.randint(1, 40, (700,), generator=g).tolist()
+    _full_check(_case("f16", None, 128, 16, 8, 2, lens, seed=4))
+
+
+def test_zero_length_sequences_give_zeros():
+    wl = _case("bf16", None, 128, 16, 16, 4, [5, 1, 300, 2], seed=5)
+    ref_k, ref_v = oracle_caches(wl)
+    sl = wl.seq_lens.clone()
+    sl[1] = 0
+    sl[3] = 0
+    ref = oracle.decode(oracle_problem(wl, ref_k, ref_v, seq_lens=sl))
+    step = GpuStep(wl)
+    step.setup(); step.write_step()
+    out = step.decode(seq_lens=sl.cuda())
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[3]) == 0
+    compare(out, ref, "bf16", "zero-length")
+
+
+def test_block_permutation_is_bit_identical():
+    wl = _case("f16", None, 128, 16, 28, 4, [37, 500, 1200, 3], seed=6)
+    step = GpuStep(wl)
+    a = step.run().clone()
+    perm = torch.randperm(wl.num_blocks, generator=torch.Generator().manual_seed(1))   # new id of block b
+    inv = torch.empty_like(perm); inv[perm] = torch.arange(wl.num_blocks)
+    d = step.dev
+    k2 = torch.empty_like(d.k_cache); v2 = torch.empty_like(d.v_cache)
+    k2[perm.cuda()] = d.k_cache; v2[perm.cuda()] = d.v_cache
+    bt = wl.block_tables.clone()
+    for i, L in enumerate(wl.seq_lens.tolist()):
+        n = -(-L // 16)
+        bt[i, :n] = perm[bt[i, :n].long()].int()
+    out = torch.empty_like(a)
+    pa.pa_decode(out, d.q, k2, v2, bt.cuda(), d.seq_lens, d.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, a)
+
+
+def test_shared_prefix_equals_copies_and_cow():
+    """Aliased table entries read exactly like private copies; the COW
+    variant's copies and writes match the oracle bit for bit."""
+    wl = inputs.prefix_share_fp16(prompt_len=200, num_prompts=3, branches=4, max_div=40,
+                                  num_q_heads=28, num_kv_heads=4, head_dim=128)
+    assert wl.cow_pairs.shape[0] == 3 * 3
+    stats, step, ref = _full_check(wl)
+    out_shared = step.out.clone()
+    # duplicate every block each sequence uses into fresh pool space
+    d = step.dev
+    lens = wl.seq_lens.tolist()
+    need = sum(-(-L // 16) for L in lens)
+    k2 = torch.cat([d.k_cache, torch.zeros((need,) + tuple(d.k_cache.shape[1:]), dtype=d.k_cache.dtype, device="cuda")])
+    v2 = torch.cat([d.v_cache, torch.zeros_like(k2[wl.num_blocks:])])
+    bt = wl.block_tables.clone()
+    nxt = wl.num_blocks
+    for i, L in enumerate(lens):
+        for j in range(-(-L // 16)):
+            b = int(bt[i, j])
+            k2[nxt] = d.k_cache[b]; v2[nxt] = d.v_cache[b]
+            bt[i, j] = nxt; nxt += 1
+    out = torch.empty_like(out_shared)
+    pa.pa_decode(out, d.q, k2, v2, bt.cuda(), d.seq_lens, d.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_shared)
+
+
+def test_bad_block_id_sets_flag_and_stays_finite():
+    wl = _case("bf16", None, 128, 16, 16, 4, [100, 200], seed=7)
+    step = GpuStep(wl)
+    step.setup(); step.write_step()
+    bt = step.dev.block_tables.clone()
+    bt[1, 3] = wl.num_blocks + 1000
+    out = step.decode(block_tables=bt)
+    torch.cuda.synchronize()
+    assert step.err.item() & pa.ERRBIT_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+
+
+def test_seq_longer_than_table_sets_flag():
+    wl = _case("f16", None, 128, 16, 8, 2, [30, 40], seed=8)
+    step = GpuStep(wl)
+    step.setup(); step.write_step()
+    sl = step.dev.seq_lens.clone()
+    sl[0] = wl.max_blocks_per_seq * 16 + 100
+    out = step.decode(seq_lens=sl)
+    torch.cuda.synchronize()
+    assert step.err.item() & pa.ERRBIT_SEQ_TOO_LONG
+    assert torch.isfinite(out.float()).all()
+
+
+def test_deterministic_and_partition_modes_agree():
+    wl = _case("bf16", None, 128, 32, 32, 8, [5000, 12000, 700], seed=9)
+    step = GpuStep(wl)
+    a = step.run().clone()
+    b = step.decode().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    c = step.decode(partition_tokens=512)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(c.float(), a.float(), atol=2e-2, rtol=2e-2)
+
+
+def test_workspace_too_small_is_rejected():
+    wl = _case("f16", None, 128, 16, 8, 2, [30], seed=10)
+    step = GpuStep(wl)
+    with pytest.raises(pa.PaError) as e:
+        step.decode(workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 3
+
+
+def test_needle_outputs_are_order_one():
+    """Peaked attention (planted keys c*q/|q|): outputs are O(1), so the
+    tolerance bites at long context."""
+    wl = inputs.make_random([3000, 9000], num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=32,
+                            kv_dtype="fp8_e4m3", q_dtype="bf16", seed=11, needles=4)
+    stats, step, ref = _full_check(wl)
+    G = 4
+    assert np.abs(ref[:, ::G]).mean() > 0.1
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled outputs, bit-exact pools, properties
+# ---------------------------------------------------------------------------
+def _sampled_check(wl, samples, seed=0, partition_tokens=0):
+    ref_k, ref_v = oracle_caches(wl)
+    step = GpuStep(wl)
+    out = step.run(partition_tokens=partition_tokens)
+    assert step.err.item() == 0
+    assert torch.isfinite(out.float()).all()
+    assert_caches_equal(step, ref_k, ref_v)
+    prob = oracle_problem(wl, ref_k, ref_v)
+    rng = np.random.default_rng(seed)
+    idx = [(int(rng.integers(wl.num_seqs)), int(rng.integers(wl.num_q_heads))) for _ in range(samples)]
+    # always include the longest sequence and the last head
+    idx.append((int(torch.argmax(wl.seq_lens)), wl.num_q_heads - 1))
+    got = torch.stack([out[i, h] for i, h in idx])
+    ref = np.stack([oracle.attend_one(prob, i, h) for i, h in idx])
+    return compare(got, ref, wl.kv_dtype, wl.name)
+
+
+@pytest.mark.slow
+def test_full_qwen7b_fp16_batch64():
+    _sampled_check(inputs.qwen7b_fp16(gen_device="cuda"), samples=48)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bs", [8, 16])
+def test_full_short_mix_bf16(bs):
+    _sampled_check(inputs.short_mix_bf16(block_size=bs, gen_device="cuda"), samples=64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("prompt_len", [2048, 2040])
+def test_full_prefix_sharing_fp16(prompt_len):
+    wl = inputs.prefix_share_fp16(prompt_len=prompt_len, gen_device="cuda")
+    assert wl.cow_pairs.shape[0] == (0 if prompt_len == 2048 else 96)
+    _sampled_check(wl, samples=48)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_full_long_context(kv):
+    _sampled_check(inputs.long_ctx(kv, gen_device="cuda"), samples=12)
+
+
+@pytest.mark.slow
+def test_full_long_context_512_token_partitions():
+    _sampled_check(inputs.long_ctx("bf16", gen_device="cuda", needles=4), samples=8, partition_tokens=512)
