@@ -45,31 +45,35 @@ def build(force: bool = False) -> str:
     return _b.build(force=force)
 
 
+def _configure(L):
+    """Declare the C signatures of include/pa.h on a loaded library."""
+    c_int, c_float, vp, sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+    L.pa_status_string.restype = ctypes.c_char_p
+    L.pa_status_string.argtypes = [c_int]
+    L.pa_last_error_detail.restype = ctypes.c_char_p
+    L.pa_last_error_detail.argtypes = []
+    L.pa_decode_workspace_size.restype = sz
+    L.pa_decode_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int]
+    dec = [vp, vp, c_int, vp, vp, c_int, vp, c_int, vp, c_int, c_int, c_int, c_int, c_int, c_int,
+           c_float, c_float, c_float, c_int, vp, sz, vp, vp]
+    for name in ("pa_decode", "pa_decode_simt"):
+        getattr(L, name).restype = c_int
+        getattr(L, name).argtypes = dec
+    L.pa_reshape_and_cache.restype = c_int
+    L.pa_reshape_and_cache.argtypes = [vp, vp, c_int, vp, vp, c_int, vp, c_int, c_int, c_int, c_int,
+                                       c_int, c_float, c_float, vp, vp]
+    L.pa_copy_blocks.restype = c_int
+    L.pa_copy_blocks.argtypes = [vp, vp, c_int, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]
+    return L
+
+
 def lib():
     """The loaded libpa.so (raises if it has not been built)."""
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libpa.so is not built ({LIB_PATH}); run paged_kv_cache_69_gb300.build()")
-        L = ctypes.CDLL(LIB_PATH)
-        c_int, c_float, vp, sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
-        L.pa_status_string.restype = ctypes.c_char_p
-        L.pa_status_string.argtypes = [c_int]
-        L.pa_last_error_detail.restype = ctypes.c_char_p
-        L.pa_last_error_detail.argtypes = []
-        L.pa_decode_workspace_size.restype = sz
-        L.pa_decode_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int]
-        dec = [vp, vp, c_int, vp, vp, c_int, vp, c_int, vp, c_int, c_int, c_int, c_int, c_int, c_int,
-               c_float, c_float, c_float, c_int, vp, sz, vp, vp]
-        for name in ("pa_decode", "pa_decode_simt"):
-            getattr(L, name).restype = c_int
-            getattr(L, name).argtypes = dec
-        L.pa_reshape_and_cache.restype = c_int
-        L.pa_reshape_and_cache.argtypes = [vp, vp, c_int, vp, vp, c_int, vp, c_int, c_int, c_int, c_int,
-                                           c_int, c_float, c_float, vp, vp]
-        L.pa_copy_blocks.restype = c_int
-        L.pa_copy_blocks.argtypes = [vp, vp, c_int, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]
-        _lib = L
+        _lib = _configure(ctypes.CDLL(LIB_PATH))
     return _lib
 
 

@@ -129,7 +129,7 @@ static size_t workspace_bytes_for(int B, int Hq, int D, int max_seq_len, int par
     const long long units = partition_tokens > 0 ? static_cast<long long>(B) * cdiv_h(max_seq_len, partition_tokens)
                                                  : static_cast<long long>(B);
     const long long slots = nr_cap + units;
-    return align256(sizeof(int2) * static_cast<size_t>(B)) + 256 +
+    return align256(sizeof(int4) * static_cast<size_t>(B)) + 256 +
            align256(sizeof(float2) * static_cast<size_t>(slots) * Hq) +
            align256(sizeof(float) * static_cast<size_t>(slots) * Hq * D);
 }
@@ -202,23 +202,44 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     DecodeParams p{};
     p.out = out; p.q = q; p.block_tables = block_tables; p.seq_lens = seq_lens; p.err_flag = err_flag;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.D = D; p.bs = bs; p.NB = NB; p.MB = MB;
+    p.out_bytes = eq;
     p.HPC = HPC; p.NHG = NHG; p.MT = MT; p.NCW = NCW;
     p.P16 = partition_tokens / 16;
     p.rpb = rpb;
     p.box_bytes = static_cast<uint32_t>(rpb * HPC * DH * 128);
     p.kv_bytes = static_cast<uint32_t>(16 * HPC * D * e);
     p.q_bytes = static_cast<uint32_t>(HPC * G * D * eq);
-    const uint32_t q_slot = (p.q_bytes + 1023u) & ~1023u;
-    p.stage_bytes = 2 * p.kv_bytes + q_slot;
+    p.q_slot_bytes = (p.q_bytes + 127u) & ~127u;
+    p.stage_bytes = 2 * p.kv_bytes;
     const uint32_t simtq = tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
-    const uint32_t extras = 2 * MAX_STAGES * 8 + MAX_STAGES * sizeof(StageDesc) + 32 * 8 + 64;
-    const long long budget = std::min(dev.max_smem, 227 * 1024) - 1024 - static_cast<long long>(simtq) - extras;
-    int stages = static_cast<int>(std::min<long long>(MAX_STAGES, budget / p.stage_bytes));
-    // keep roughly 160 KB of K/V in flight per CTA; more stages buy nothing
-    stages = std::min(stages, std::max(2, static_cast<int>((160 * 1024) / p.stage_bytes)));
+    const uint32_t extras = 1024;   // barriers, stage descriptors, prologue scratch
+    const uint32_t fixed = NQ * p.q_slot_bytes + simtq + extras + 1024;   // + base alignment slack
+    const int threads = (NCW + 1) * 32;
+    // Two co-resident CTAs per SM double the consumer warps that hide the
+    // per-chunk MMA/softmax latency; use them when registers and shared
+    // memory allow at least 3 stages each, else one CTA with a deeper ring.
+    cudaFuncAttributes fa{};
+    cudaError_t ce = cudaFuncGetAttributes(&fa, kern);
+    if (ce != cudaSuccess) return fail_cuda("decode: kernel attributes", ce);
+    const int regs = (fa.numRegs + 7) & ~7;
+    const int by_regs = std::max(1, 65536 / std::max(1, regs * threads));
+    const long long sm_smem = std::min(dev.max_smem, 227 * 1024) + 1024LL;   // per-SM budget incl. reservation
+    int stages = 0;
+    if (by_regs >= 2) {
+        const long long per_cta = sm_smem / 2 - 1024 - fixed;
+        const int s2 = static_cast<int>(std::min<long long>(MAX_STAGES, per_cta / p.stage_bytes));
+        if (s2 >= 3) stages = s2;
+    }
+    if (stages == 0) {
+        const long long per_cta = std::min(dev.max_smem, 227 * 1024) - static_cast<long long>(fixed);
+        stages = static_cast<int>(std::min<long long>(MAX_STAGES, per_cta / p.stage_bytes));
+        // roughly 160 KB of K/V in flight per CTA; more stages buy nothing
+        stages = std::min(stages, std::max(2, static_cast<int>((160 * 1024) / p.stage_bytes)));
+    }
     if (stages < 2) return fail(PA_ERR_UNSUPPORTED, "decode: pipeline stages do not fit in shared memory");
     p.stages = stages;
-    p.simtq_off = stages * p.stage_bytes;
+    p.q_off = stages * p.stage_bytes;
+    p.simtq_off = p.q_off + NQ * p.q_slot_bytes;
     p.bar_off = (p.simtq_off + simtq + 15u) & ~15u;
     const size_t smem = 1024 + p.bar_off + extras;
     const float log2e = 1.4426950408889634f;
@@ -231,7 +252,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     if (workspace_bytes < need) return fail(PA_ERR_WORKSPACE, "decode: workspace smaller than pa_decode_workspace_size()");
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PA_ERR_WORKSPACE, "decode: workspace must be 256-byte aligned");
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.seq_info = reinterpret_cast<int2*>(ws); ws += align256(sizeof(int2) * static_cast<size_t>(B));
+    p.split_list = reinterpret_cast<int4*>(ws); ws += align256(sizeof(int4) * static_cast<size_t>(B));
     p.totals = reinterpret_cast<int*>(ws); ws += 256;
     p.max_slots = max_slots_for(B, MB * bs, partition_tokens, dev.sms);
     p.part_ml = reinterpret_cast<float2*>(ws); ws += align256(sizeof(float2) * static_cast<size_t>(p.max_slots) * Hq);
@@ -254,8 +275,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     }
 
     // grid: persistent CTAs, as many as fit, split into ranges x head groups
-    const int threads = (NCW + 1) * 32;
-    cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (ce != cudaSuccess) return fail_cuda("decode: set shared memory size", ce);
     int per_sm = 0;
     ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
@@ -263,7 +283,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     per_sm = std::max(1, per_sm);
     const long long chunk_bound = static_cast<long long>(B) * cdiv_h(static_cast<long long>(MB) * bs, 16);
     long long NR = std::max(1LL, static_cast<long long>(per_sm) * dev.sms / NHG);
-    NR = std::min(NR, 2LL * dev.sms);
+    NR = std::min(NR, 2LL * dev.sms);   // the workspace holds 2 x SMs ranges
     NR = std::min(NR, chunk_bound);
     p.NR = static_cast<int>(NR);
 
@@ -280,8 +300,17 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg{};
-    rcfg.gridDim = dim3(static_cast<unsigned>(B));
-    rcfg.blockDim = dim3(256);
+    {
+        // persistent reduce grid: one wave of CTAs striding over the
+        // (split sequence, head group) items
+        int red_per_sm = 0;
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&red_per_sm, rkern, RED_THREADS, 0);
+        if (ce != cudaSuccess) return fail_cuda("decode: reduce occupancy query", ce);
+        const long long items = static_cast<long long>(B) * ((Hq + RED_THREADS / 32 - 1) / (RED_THREADS / 32));
+        const long long g = std::max(1LL, std::min(items, static_cast<long long>(std::max(1, red_per_sm)) * dev.sms));
+        rcfg.gridDim = dim3(static_cast<unsigned>(g));
+    }
+    rcfg.blockDim = dim3(RED_THREADS);
     rcfg.dynamicSmemBytes = 0;
     rcfg.stream = stream;
     rcfg.attrs = attr;

@@ -37,6 +37,7 @@ namespace pa {
 
 constexpr int CHUNK = 16;            // tokens per pipeline stage
 constexpr int MAX_STAGES = 8;
+constexpr int NQ = 2;                // query-row ring slots
 constexpr int MAX_WARPS = 9;         // up to 8 consumers + 1 producer
 
 enum : uint32_t { SEG_START = 1u, SEG_END = 2u, DIRECT = 4u };
@@ -47,7 +48,8 @@ struct StageDesc {
     int slot;
     uint32_t vmask;
     uint32_t flags;
-    int pad[3];
+    int qslot;               // query ring slot holding this segment's rows
+    int pad[2];
 };
 
 struct DecodeParams {
@@ -57,10 +59,11 @@ struct DecodeParams {
     const int32_t* seq_lens;
     float* part_acc;          // [max_slots][Hq][D]
     float2* part_ml;          // [max_slots][Hq]  (m in log2 units, l)
-    int2* seq_info;           // [B] (first chunk, first unit)
-    int* totals;              // [0] chunks, [1] units
+    int4* split_list;         // [B] (seq, first chunk, first unit, length) of sequences needing a merge
+    int* totals;              // [0] chunks, [1] units, [2] entries in split_list
     int32_t* err_flag;
     int B, Hq, Hkv, G, D, bs, NB, MB;
+    int out_bytes;            // bytes of one output element
     int HPC, NHG, NR, MT, NCW;
     int P16;                  // partition length in chunks, 0 = none
     int max_slots;
@@ -71,7 +74,9 @@ struct DecodeParams {
     uint32_t box_bytes;       // bytes of one K (or V) box
     uint32_t kv_bytes;        // bytes of one stage's K (or V) buffer
     uint32_t q_bytes;         // query bytes copied per segment start
-    uint32_t stage_bytes;     // K + V + Q slot
+    uint32_t q_slot_bytes;    // one query ring slot
+    uint32_t stage_bytes;     // K + V
+    uint32_t q_off;           // offset of the query ring
     uint32_t simtq_off;       // offset of the CUDA-core private query rows
     uint32_t bar_off;         // offset of the barriers
     int per_head_copies;      // 1: one TMA copy per (head, 128-B column block)
@@ -89,11 +94,15 @@ __device__ __forceinline__ int n_units(int L, int P16) {
 // The range (CTA column) owning global chunk c: largest r with
 // floor(r * C / NR) <= c.
 __device__ __forceinline__ int range_of(int c, int C, int NR) {
+    if (static_cast<long long>(C) * NR < 0x7fffffffLL)       // 32-bit division when it cannot overflow
+        return static_cast<int>((static_cast<unsigned>(c + 1) * static_cast<unsigned>(NR) - 1u) /
+                                static_cast<unsigned>(C));
     return static_cast<int>(((static_cast<long long>(c) + 1) * NR - 1) / C);
 }
 // Range r covers chunks [floor(r*C/NR), floor((r+1)*C/NR)); with more
 // ranges than chunks some are empty and write no partial.
 __device__ __forceinline__ bool range_empty(int r, int C, int NR) {
+    if (C >= NR) return false;                                // every range holds a chunk
     return static_cast<long long>(r) * C / NR == (static_cast<long long>(r) + 1) * C / NR;
 }
 
@@ -135,6 +144,7 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
         usum += n_units(L, p.P16);
     }
     if (bad && blockIdx.x == 0) raise_flag(p.err_flag, PA_ERRBIT_SEQ_TOO_LONG);
+    if (blockIdx.x == 0 && tid == 0) p.totals[2] = 0;
     int ci = csum, ui = usum;           // inclusive within the warp
     warp_scan_pair(ci, ui);
     if (lane == 31) scratch[warp] = make_int2(ci, ui);
@@ -164,12 +174,21 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
         }
     }
     if (blockIdx.x == 0) {
+        // Sequences split across ranges or partitions go to the merge list;
+        // empty sequences get zero outputs here.
         int S = cpre, U = upre;
         for (int i = i0; i < i1; ++i) {
-            p.seq_info[i] = make_int2(S, U);
             const int L = clamp_len(p.seq_lens[i], maxL);
-            S += cdiv_i(L, CHUNK);
-            U += n_units(L, p.P16);
+            const int n16 = cdiv_i(L, CHUNK), nu = n_units(L, p.P16);
+            if (L == 0) {
+                uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                                    static_cast<size_t>(i) * p.Hq * p.D * p.out_bytes);
+                for (int k = 0; k < p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
+            } else if (!(nu == 1 && range_of(S, C, p.NR) == range_of(S + n16 - 1, C, p.NR))) {
+                p.split_list[atomicAdd(&p.totals[2], 1)] = make_int4(i, S, U, L);
+            }
+            S += n16;
+            U += nu;
         }
         if (tid == 0) { p.totals[0] = C; p.totals[1] = Ut; }
     }
@@ -213,7 +232,7 @@ struct DecodeKernel {
 
     // ---------------- producer ----------------
     static __device__ void producer(const DecodeParams& p, const Plan& pl, int hg, uint8_t* base,
-                                    uint64_t* full, uint64_t* empty, StageDesc* descs,
+                                    uint64_t* full, uint64_t* empty, uint64_t* qempty, StageDesc* descs,
                                     const CUtensorMap* tk, const CUtensorMap* tv) {
         const int lane = threadIdx.x & 31;
         const int S = p.stages;
@@ -225,7 +244,7 @@ struct DecodeKernel {
         int wbase = INT_MIN / 2, wval = -1;
         const int nb = p.bs >= CHUNK ? 1 : CHUNK / p.bs;      // boxes per chunk
         const int hq0 = hg * p.HPC * p.G;
-        int issued = 0;
+        int issued = 0, qcount = 0;
         bool ok = true;
         for (int k = pl.cs; k < pl.ce; ++k) {
             while (j >= n16) {
@@ -247,6 +266,13 @@ struct DecodeKernel {
                 const int slot = issued % S;
                 const uint32_t round = issued / S;
                 if (issued >= S && !mbar_wait_bounded(&empty[slot], (round - 1) & 1u)) {
+                    raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                    ok = false;
+                }
+                const bool seg_start = (k == pl.cs) || (j == 0) || (p.P16 > 0 && j % p.P16 == 0);
+                const int qs = qcount % NQ;
+                if (ok && seg_start && qcount >= NQ &&
+                    !mbar_wait_bounded(&qempty[qs], ((qcount / NQ) - 1) & 1u)) {
                     raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
                     ok = false;
                 }
@@ -272,7 +298,6 @@ struct DecodeKernel {
                         ++nbox_issued;
                     }
                     uint32_t flags = 0;
-                    const bool seg_start = (k == pl.cs) || (j == 0) || (p.P16 > 0 && j % p.P16 == 0);
                     const bool seg_end = (k == pl.ce - 1) || (j == n16 - 1) ||
                                          (p.P16 > 0 && (j + 1) % p.P16 == 0);
                     if (seg_start) flags |= SEG_START;
@@ -282,6 +307,7 @@ struct DecodeKernel {
                     StageDesc d;
                     d.seq = i; d.tok0 = tok0; d.vmask = vmask; d.flags = flags;
                     d.slot = (blockIdx.x / p.NHG) + Ui + (p.P16 > 0 ? j / p.P16 : 0);
+                    d.qslot = qs;
                     descs[slot] = d;
                     const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (seg_start ? p.q_bytes : 0u);
                     mbar_arrive_expect_tx(&full[slot], bytes);
@@ -307,7 +333,8 @@ struct DecodeKernel {
                     if (seg_start) {
                         const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
                             (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
-                        bulk_load(kbuf + 2 * p.kv_bytes, qsrc, p.q_bytes, &full[slot]);
+                        bulk_load(base + p.q_off + qs * p.q_slot_bytes, qsrc, p.q_bytes, &full[slot]);
+                        ++qcount;
                     }
                 }
             }
@@ -347,7 +374,7 @@ struct DecodeKernel {
 
     // ---------------- tensor-core consumer ----------------
     static __device__ void consumer_tc(const DecodeParams& p, const Plan& pl, int hg, int w,
-                                       uint8_t* base, uint64_t* full, uint64_t* empty,
+                                       uint8_t* base, uint64_t* full, uint64_t* empty, uint64_t* qempty,
                                        const StageDesc* descs) {
         const int lane = threadIdx.x & 31;
         const int g4 = lane >> 2, t4 = lane & 3;
@@ -377,9 +404,10 @@ struct DecodeKernel {
             const StageDesc d = descs[slot];
             uint8_t* kbuf = base + slot * p.stage_bytes;
             uint8_t* vbuf = kbuf + p.kv_bytes;
-            const uint8_t* qbuf = kbuf + 2 * p.kv_bytes;
             if (d.flags & SEG_START) {
-                load_q_frags(qa, qbuf, qrow_lo, rows_valid, lane);
+                load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo, rows_valid, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
                 m0 = m1 = -INFINITY; l0 = l1 = 0.f;
@@ -400,23 +428,38 @@ struct DecodeKernel {
             float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             const uint32_t kb = smem_u32(kbuf);
             if constexpr (!FP8) {
+                // two accumulator chains per tile (even / odd k-steps) halve the
+                // dependent-MMA latency of the chunk
+                float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t b0, b1, b2, b3;
+                for (int ks = 0; ks < KS; ks += 2) {
+                    uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
                     ldsm_x4(kb + lay.chunk_addr(rbK, tokK, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+                    ldsm_x4(kb + lay.chunk_addr(rbK, tokK, 2 * ks + 2 + (mi & 1)), c0, c1, c2, c3);
                     mma_16816<MMA_BF16>(s[0], qa[ks], b0, b1);
                     mma_16816<MMA_BF16>(s[1], qa[ks], b2, b3);
+                    mma_16816<MMA_BF16>(s2[0], qa[ks + 1], c0, c1);
+                    mma_16816<MMA_BF16>(s2[1], qa[ks + 1], c2, c3);
                 }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
             } else {
+                float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < KS; ks += 2) {
                     uint32_t r0, r1, r2, r3;    // (tile0,ks) (tile0,ks+1) (tile1,ks) (tile1,ks+1)
                     ldsm_x4(kb + lay.chunk_addr(rbK, tokK, ks + (mi & 1)), r0, r1, r2, r3);
                     mma_16816<false>(s[0], qa[ks], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
-                    mma_16816<false>(s[0], qa[ks + 1], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+                    mma_16816<false>(s2[0], qa[ks + 1], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
                     mma_16816<false>(s[1], qa[ks], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
-                    mma_16816<false>(s[1], qa[ks + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+                    mma_16816<false>(s2[1], qa[ks + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
                 }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
             }
             // ---- online softmax (log2 domain), rows g4 and g4+8 ----
 #pragma unroll
@@ -579,7 +622,7 @@ struct DecodeKernel {
     // token t over half of head_dim for up to 16 query rows; for P*V each
     // lane owns D/32 consecutive columns.
     static __device__ void consumer_simt(const DecodeParams& p, const Plan& pl, int hg, int w,
-                                         uint8_t* base, uint64_t* full, uint64_t* empty,
+                                         uint8_t* base, uint64_t* full, uint64_t* empty, uint64_t* qempty,
                                          const StageDesc* descs, float* qpriv) {
         constexpr int R = 16;
         constexpr int VE = 16 / KV::bytes;     // elements per 16-byte chunk
@@ -606,10 +649,12 @@ struct DecodeKernel {
             const StageDesc d = descs[slot];
             const uint8_t* kbuf = base + slot * p.stage_bytes;
             const uint8_t* vbuf = kbuf + p.kv_bytes;
-            const QE* qbuf = reinterpret_cast<const QE*>(kbuf + 2 * p.kv_bytes);
             if (d.flags & SEG_START) {
+                const QE* qbuf = reinterpret_cast<const QE*>(base + p.q_off + d.qslot * p.q_slot_bytes);
                 for (int e = lane; e < nr * D; e += 32)
                     qp[e] = to_float(qbuf[static_cast<size_t>(qrow_lo) * D + e]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     m[r] = -INFINITY; l[r] = 0.f;
@@ -767,7 +812,8 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + p.bar_off);
     uint64_t* empty = full + MAX_STAGES;
-    StageDesc* descs = reinterpret_cast<StageDesc*>(empty + MAX_STAGES);
+    uint64_t* qempty = empty + MAX_STAGES;
+    StageDesc* descs = reinterpret_cast<StageDesc*>(qempty + 2 * NQ);
     int2* scratch = reinterpret_cast<int2*>(descs + MAX_STAGES);
     int4* s_first = reinterpret_cast<int4*>(scratch + 32);
     int2* s_tot = reinterpret_cast<int2*>(s_first + 1);
@@ -776,6 +822,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     const int range = blockIdx.x / p.NHG;
     Plan pl;
     make_plan(p, range, scratch, s_first, s_tot, pl);
+    grid_dependents_launch();     // the reduce kernel may start its own prologue
     if (pl.cs >= pl.ce || pl.seq < 0) return;
 
     const int warp = threadIdx.x >> 5;
@@ -784,84 +831,123 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], p.NCW);
         }
+        for (int s = 0; s < NQ; ++s) mbar_init(&qempty[s], p.NCW);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     __syncthreads();
     if (warp == p.NCW) {
         if ((threadIdx.x & 31) == 0) { prefetch_tensormap(&tk); prefetch_tensormap(&tv); }
-        K::producer(p, pl, hg, base, full, empty, descs, &tk, &tv);
+        K::producer(p, pl, hg, base, full, empty, qempty, descs, &tk, &tv);
     } else if (warp < p.NCW) {
         if constexpr (TC) {
-            K::consumer_tc(p, pl, hg, warp, base, full, empty, descs);
+            K::consumer_tc(p, pl, hg, warp, base, full, empty, qempty, descs);
         } else {
-            K::consumer_simt(p, pl, hg, warp, base, full, empty, descs,
+            K::consumer_simt(p, pl, hg, warp, base, full, empty, qempty, descs,
                              reinterpret_cast<float*>(base + p.simtq_off));
         }
     }
-    grid_dependents_launch();
 }
 
 // ---------------------------------------------------------------------------
 // log-sum-exp merge of the partials of sequences split across CTAs or
 // partitions:  M = max m_k,  out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
-// One CTA per sequence, one warp per head at a time, lanes over head_dim.
+// One warp per (sequence, head); lanes own head_dim/32 consecutive columns.
+// Partials of one sequence lie at slots range + first_unit + unit.
 // ---------------------------------------------------------------------------
-template <typename OutT, int D>
-__global__ void __launch_bounds__(256)
-pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
-    grid_dependency_wait();
-    const int i = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int L = clamp_len(p.seq_lens[i], p.MB * p.bs);
-    OutT* out = static_cast<OutT*>(p.out) + static_cast<size_t>(i) * p.Hq * D;
-    constexpr int DPL = D / 32;
-    if (L == 0) {
-        for (int e = threadIdx.x; e < p.Hq * D; e += blockDim.x) out[e] = from_float<OutT>(0.f);
-        return;
+// Read-only vector loads as ordered inline PTX: a batch of them issues back
+// to back instead of being sunk next to each use.
+template <int DPL>
+struct VecF;
+template <> struct VecF<4> {
+    static __device__ __forceinline__ void load(const float* p, float (&v)[4]) {
+        asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "l"(p));
     }
-    const int2 info = p.seq_info[i];
-    const int C = p.totals[0];
-    const int n16 = cdiv_i(L, CHUNK), nu = n_units(L, p.P16);
-    if (nu == 1 && range_of(info.x, C, p.NR) == range_of(info.x + n16 - 1, C, p.NR)) return;
-    for (int h = warp; h < p.Hq; h += nw) {
-        // pass 1: the running maximum over every partial of (i, h)
-        float M = -INFINITY;
-        for (int u = 0; u < nu; ++u) {
-            const int a = info.x + (p.P16 > 0 ? u * p.P16 : 0);
-            const int b = p.P16 > 0 ? min(a + p.P16, info.x + n16) : info.x + n16;
-            const int r0 = range_of(a, C, p.NR), r1 = range_of(b - 1, C, p.NR);
-            for (int r = r0 + lane; r <= r1; r += 32) {
-                if (range_empty(r, C, p.NR)) continue;
-                const int slot = r + info.y + u;
-                if (slot < p.max_slots) M = fmaxf(M, p.part_ml[static_cast<size_t>(slot) * p.Hq + h].x);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float Mu = (M == -INFINITY) ? 0.f : M;
+};
+template <> struct VecF<2> {
+    static __device__ __forceinline__ void load(const float* p, float (&v)[2]) {
+        asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "l"(p));
+    }
+};
+
+constexpr int RED_THREADS = 128;     // 4 warps: one query head each
+
+template <typename OutT, int D>
+__global__ void __launch_bounds__(RED_THREADS)
+pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int DPL = D / 32;
+    constexpr int NB = 16;               // partials whose rows load together
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int HG = cdiv_i(p.Hq, nw);     // head groups of nw heads
+    grid_dependency_wait();
+    for (int item = blockIdx.x;; item += gridDim.x) {
+        // the count and this item's list entry load together
+        // the count, the chunk total and this item's list entry load together
+        const int count = *reinterpret_cast<volatile int*>(&p.totals[2]);
+        const int C = p.totals[0];
+        const int4 e = p.split_list[min(item / HG, p.B - 1)];
+        if (item >= count * HG) break;
+        const int h = (item % HG) * nw + warp;
+        if (h >= p.Hq) continue;
+        const int i = e.x, S = e.y, U = e.z, L = e.w;
+        const int n16 = cdiv_i(L, CHUNK), nu = n_units(L, p.P16);
+        OutT* o = static_cast<OutT*>(p.out) + (static_cast<size_t>(i) * p.Hq + h) * D + lane * DPL;
         float num[DPL];
 #pragma unroll
         for (int c = 0; c < DPL; ++c) num[c] = 0.f;
-        float den = 0.f;
+        float den = 0.f, M = -INFINITY;
+        // Up to NB partials per batch, one per lane: their (m, l) and their
+        // accumulator rows are independent loads issued together.
+        auto merge = [&](int n, int my_slot) {
+            float2 ml = make_float2(-INFINITY, 0.f);
+            if (lane < n) ml = p.part_ml[static_cast<size_t>(my_slot) * p.Hq + h];
+            float v[NB][DPL];
+#pragma unroll
+            for (int t = 0; t < NB; ++t) {
+                const int st = __shfl_sync(0xffffffffu, my_slot, t);
+                if (t < n) {
+                    VecF<DPL>::load(p.part_acc + (static_cast<size_t>(st) * p.Hq + h) * D + lane * DPL, v[t]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) v[t][c] = 0.f;
+                }
+            }
+            float bm = ml.x;
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o2));
+            const float Mn = fmaxf(M, bm);
+            const float Mu = (Mn == -INFINITY) ? 0.f : Mn;
+            const float sold = exp2f(M - Mu);
+            const float w = lane < n ? exp2f(ml.x - Mu) : 0.f;
+            float wl = w * ml.y;
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o2);
+            den = den * sold + wl;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) num[c] *= sold;
+#pragma unroll
+            for (int t = 0; t < NB; ++t) {
+                const float wt = __shfl_sync(0xffffffffu, w, t);
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) num[c] = fmaf(wt, v[t][c], num[c]);
+            }
+            M = Mn;
+        };
+        int cnt = 0, my_slot = 0;
         for (int u = 0; u < nu; ++u) {
-            const int a = info.x + (p.P16 > 0 ? u * p.P16 : 0);
-            const int b = p.P16 > 0 ? min(a + p.P16, info.x + n16) : info.x + n16;
+            const int a = S + (p.P16 > 0 ? u * p.P16 : 0);
+            const int b = p.P16 > 0 ? min(a + p.P16, S + n16) : S + n16;
             const int r0 = range_of(a, C, p.NR), r1 = range_of(b - 1, C, p.NR);
             for (int r = r0; r <= r1; ++r) {
-                if (range_empty(r, C, p.NR)) continue;
-                const int slot = r + info.y + u;
-                if (slot >= p.max_slots) continue;
-                const float2 ml = p.part_ml[static_cast<size_t>(slot) * p.Hq + h];
-                const float wgt = exp2f(ml.x - Mu);
-                den = fmaf(wgt, ml.y, den);
-                const float* src = p.part_acc + (static_cast<size_t>(slot) * p.Hq + h) * D + lane * DPL;
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) num[c] = fmaf(wgt, src[c], num[c]);
+                const int slot = r + U + u;
+                if (range_empty(r, C, p.NR) || slot >= p.max_slots) continue;
+                if ((cnt % NB) == lane) my_slot = slot;
+                if ((++cnt % NB) == 0) merge(NB, my_slot);
             }
         }
+        if (cnt % NB) merge(cnt % NB, my_slot);
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        OutT* o = out + static_cast<size_t>(h) * D + lane * DPL;
 #pragma unroll
         for (int c = 0; c < DPL; ++c) o[c] = from_float<OutT>(num[c] * inv);
     }

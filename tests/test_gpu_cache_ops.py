@@ -1,5 +1,7 @@
 """GPU parity of the cache write and the block copy: bit-exact against the
 oracle, through the C-ABI."""
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -24,8 +26,8 @@ def _pool(NB, bs, Hkv, D, dtype):
                                     ("fp8_e4m3", "f32"), ("fp8_e4m3", "f16"), ("fp8_e4m3", "bf16")])
 @pytest.mark.parametrize("Hkv,D,bs", [(2, 64, 16), (8, 128, 8), (4, 128, 32)])
 def test_reshape_and_cache_bit_exact(kv, src, Hkv, D, bs):
-    NB, T = 37, 300
-    g = torch.Generator().manual_seed(hash((kv, src, Hkv, D, bs)) & 0xffff)
+    NB, T = 64, 300
+    g = torch.Generator().manual_seed(zlib.crc32(repr((kv, src, Hkv, D, bs)).encode()) & 0xffff)
     key = (torch.randn(T, Hkv, D, generator=g) * 3).to(inputs.STORAGE[src])
     val = (torch.randn(T, Hkv, D, generator=g) * 3).to(inputs.STORAGE[src])
     key[0, 0, :3] = torch.tensor([float("nan"), float("inf"), -1e6]).to(key.dtype)

@@ -165,7 +165,11 @@ def test_seq_longer_than_table_sets_flag():
     out = step.decode(seq_lens=sl)
     torch.cuda.synchronize()
     assert step.err.item() & pa.ERRBIT_SEQ_TOO_LONG
-    assert torch.isfinite(out.float()).all()
+    # the over-long sequence is clamped to its table and may read unused
+    # (NaN-filled) slots; the other sequence is unaffected
+    ref_k, ref_v = oracle_caches(wl)
+    ref = oracle.decode(oracle_problem(wl, ref_k, ref_v))
+    compare(out[1:], ref[1:], "f16", "neighbour of an over-long sequence")
 
 
 def test_deterministic_and_partition_modes_agree():
