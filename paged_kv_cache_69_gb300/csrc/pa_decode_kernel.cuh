@@ -870,6 +870,11 @@ template <> struct VecF<2> {
         asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "l"(p));
     }
 };
+__device__ __forceinline__ float2 ldg_f2(const float2* p) {
+    float2 v;
+    asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
 
 constexpr int RED_THREADS = 128;     // 4 warps: one query head each
 
@@ -897,6 +902,51 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
         for (int c = 0; c < DPL; ++c) num[c] = 0.f;
         float den = 0.f, M = -INFINITY;
+        if (p.P16 == 0 && C >= p.NR) {
+            // Common case: the partials are the consecutive slots of ranges
+            // r0..r1.  Every lane loads all (m, l) pairs (broadcast) and its
+            // columns of each partial at once, then merges locally.
+            const int r0 = range_of(S, C, p.NR), r1 = range_of(S + n16 - 1, C, p.NR);
+            const int base = r0 + U;
+            const int n = min(r1 - r0 + 1, p.max_slots - base);
+            for (int b0 = 0; b0 < n; b0 += NB) {
+                float2 ml[NB];
+                float v[NB][DPL];
+#pragma unroll
+                for (int t = 0; t < NB; ++t)
+                    ml[t] = (b0 + t < n) ? ldg_f2(p.part_ml + static_cast<size_t>(base + b0 + t) * p.Hq + h)
+                                         : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int t = 0; t < NB; ++t) {
+                    if (b0 + t < n) {
+                        VecF<DPL>::load(p.part_acc + (static_cast<size_t>(base + b0 + t) * p.Hq + h) * D + lane * DPL, v[t]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < DPL; ++c) v[t][c] = 0.f;
+                    }
+                }
+                float Mn = M;
+#pragma unroll
+                for (int t = 0; t < NB; ++t) Mn = fmaxf(Mn, ml[t].x);
+                const float Mu = (Mn == -INFINITY) ? 0.f : Mn;
+                const float sold = exp2f(M - Mu);
+                den *= sold;
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) num[c] *= sold;
+#pragma unroll
+                for (int t = 0; t < NB; ++t) {
+                    const float wt = exp2f(ml[t].x - Mu);      // 0 for padding (m = -inf)
+                    den = fmaf(wt, ml[t].y, den);
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) num[c] = fmaf(wt, v[t][c], num[c]);
+                }
+                M = Mn;
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) o[c] = from_float<OutT>(num[c] * inv);
+            continue;
+        }
         // Up to NB partials per batch, one per lane: their (m, l) and their
         // accumulator rows are independent loads issued together.
         auto merge = [&](int n, int my_slot) {
