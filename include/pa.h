@@ -138,6 +138,33 @@ pa_status pa_decode_simt(void* out, const void* q, pa_dtype q_dtype,
                          int32_t* err_flag, cudaStream_t stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot supply a workspace.
+ * The pages have no counterpart: this exists for callers that must not
+ * allocate device memory on the call path, such as a serving loop whose
+ * memory is fully pre-partitioned by its own allocator, or a plugin inside a
+ * host framework that owns all device memory.  Arguments and results are
+ * those of pa_decode without the workspace; the split-KV partials go to a
+ * scratch array of PA_NOALLOC_SCRATCH_BYTES that the library keeps in device
+ * memory on every GPU it is loaded on, until the process exits.
+ *   - The first call on a device looks up the array's address on that device
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - A batch needing more scratch than PA_NOALLOC_SCRATCH_BYTES (see
+ *     pa_decode_workspace_size) returns PA_ERR_WORKSPACE and launches nothing.
+ *   - All calls on a device share the array and it keeps the previous call's
+ *     contents; calls whose GPU work overlaps race on it.  No contents need
+ *     to start at zero.
+ *   - Nothing is allocated or freed.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+pa_status pa_decode_noalloc(void* out, const void* q, pa_dtype q_dtype,
+                            const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, float k_scale, float v_scale,
+                            int partition_tokens, int32_t* err_flag, cudaStream_t stream);
+
+/*
  * pa_reshape_and_cache -- write token t's K and V rows ([num_kv_heads,
  * head_dim] each) into pool slot slot_mapping[t] ("vLLM intro part 2",
  * section 3.2, slot_mapping; "kv-cache-memory-core", section 3, decode

@@ -24,7 +24,8 @@ ERRBIT_BAD_BLOCK, ERRBIT_BAD_SLOT, ERRBIT_BAD_PAIR, ERRBIT_SEQ_TOO_LONG, ERRBIT_
 
 # entry points declared in include/pa.h
 EXPORTED = ("pa_status_string", "pa_last_error_detail", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_simt", "pa_reshape_and_cache", "pa_copy_blocks")
+            "pa_decode_simt", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _DTYPE_CODE = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16,
                torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: PA_FP8_E4M3}
@@ -59,6 +60,8 @@ def _configure(L):
     for name in ("pa_decode", "pa_decode_simt"):
         getattr(L, name).restype = c_int
         getattr(L, name).argtypes = dec
+    L.pa_decode_noalloc.restype = c_int
+    L.pa_decode_noalloc.argtypes = dec[:19] + [vp, vp]
     L.pa_reshape_and_cache.restype = c_int
     L.pa_reshape_and_cache.argtypes = [vp, vp, c_int, vp, vp, c_int, vp, c_int, c_int, c_int, c_int,
                                        c_int, c_float, c_float, vp, vp]
@@ -153,6 +156,27 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
               _ptr(block_tables), MB, _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, float(scale),
               float(k_scale), float(v_scale), int(partition_tokens), _ptr(workspace),
               workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
+    return out
+
+
+def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, kv_dtype=None, *,
+                      k_scale: float = 1.0, v_scale: float = 1.0, partition_tokens: int = 0,
+                      err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_decode without a workspace argument, for callers that cannot
+    allocate one: the partials go to the library's built-in device scratch
+    (NOALLOC_SCRATCH_BYTES per GPU, shared by all calls on that GPU)."""
+    _dev(out, q, k_cache, v_cache, block_tables, seq_lens, err_flag)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(out.shape) != (B, Hq, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out, k_cache and v_cache")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    _check(lib().pa_decode_noalloc(_ptr(out), _ptr(q), _code(q), _ptr(k_cache), _ptr(v_cache),
+                                   _code(k_cache, kv_dtype), _ptr(block_tables), block_tables.shape[1],
+                                   _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, float(scale), float(k_scale),
+                                   float(v_scale), int(partition_tokens), _ptr(err_flag), _stream(stream)))
     return out
 
 
