@@ -209,7 +209,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.box_bytes = static_cast<uint32_t>(rpb * HPC * DH * 128);
     p.kv_bytes = static_cast<uint32_t>(16 * HPC * D * e);
     p.q_bytes = static_cast<uint32_t>(HPC * G * D * eq);
-    p.q_slot_bytes = (p.q_bytes + 127u) & ~127u;
+    p.q_slot_bytes = (p.q_bytes + 1023u) & ~1023u;   // swizzled tensor copies need 1024-B alignment
     p.stage_bytes = 2 * p.kv_bytes;
     const uint32_t simtq = tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
     const uint32_t extras = 1024;   // barriers, stage descriptors, prologue scratch
@@ -274,6 +274,26 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         }
     }
 
+    // query rows: a 128-B-swizzled tensor copy [column block][row][128 B] of
+    // the CTA's HPC*G rows, so the MMA fragment loads are bank-conflict free
+    alignas(64) CUtensorMap tq;
+    std::memset(&tq, 0, sizeof tq);
+    p.q_tma = 0;
+    if (tc) {
+        const EncodeTiledFn enc = encode_fn();
+        const cuuint32_t e128q = static_cast<cuuint32_t>(128 / eq);
+        const cuuint32_t dhq = static_cast<cuuint32_t>(D * eq / 128);
+        cuuint64_t dims[3] = {e128q, static_cast<cuuint64_t>(B) * Hq, dhq};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * eq, 128};
+        cuuint32_t box[3] = {e128q, static_cast<cuuint32_t>(HPC * G), dhq};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc && HPC * G <= 256 &&
+            enc(&tq, tmap_type(q_dtype), 3, const_cast<void*>(q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            p.q_tma = 1;
+    }
+
     // grid: persistent CTAs, as many as fit, split into ranges x head groups
     ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (ce != cudaSuccess) return fail_cuda("decode: set shared memory size", ce);
@@ -292,7 +312,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    void* args[] = {&p, &tk, &tv};
+    void* args[] = {&p, &tk, &tv, &tq};
     ce = cudaLaunchKernelExC(&cfg, kern, args);
     if (ce != cudaSuccess) return fail_cuda("decode: main kernel launch", ce);
 

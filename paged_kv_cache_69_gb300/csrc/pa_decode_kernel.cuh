@@ -80,6 +80,7 @@ struct DecodeParams {
     uint32_t simtq_off;       // offset of the CUDA-core private query rows
     uint32_t bar_off;         // offset of the barriers
     int per_head_copies;      // 1: one TMA copy per (head, 128-B column block)
+    int q_tma;                // 1: query rows arrive by a 128-B-swizzled tensor copy
 };
 
 __device__ __forceinline__ int cdiv_i(int a, int b) { return (a + b - 1) / b; }
@@ -219,6 +220,18 @@ struct KVLayout {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// Four consecutive output values in one vector store.
+template <typename T> __device__ __forceinline__ void store4(T* dst, const float (&v)[4]);
+template <> __device__ __forceinline__ void store4<float>(float* dst, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <> __device__ __forceinline__ void store4<__half>(__half* dst, const float (&v)[4]) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v[0], v[1], false), pack2(v[2], v[3], false));
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[4]) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v[0], v[1], true), pack2(v[2], v[3], true));
+}
+
 template <class KV, class QT, int D, bool TC>
 struct DecodeKernel {
     using KT = typename KV::T;
@@ -233,31 +246,67 @@ struct DecodeKernel {
     // ---------------- producer ----------------
     static __device__ void producer(const DecodeParams& p, const Plan& pl, int hg, uint8_t* base,
                                     uint64_t* full, uint64_t* empty, uint64_t* qempty, StageDesc* descs,
-                                    const CUtensorMap* tk, const CUtensorMap* tv) {
+                                    const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq) {
         const int lane = threadIdx.x & 31;
         const int S = p.stages;
         const int maxL = p.MB * p.bs;
+        // Sequence lengths come 32 sequences per warp-wide load, and block
+        // table entries in 32-entry windows with the window after the
+        // current one always in flight, so neither a change of sequence nor
+        // a long sequence stalls the copy issue on a dependent global load.
+        int lbase = pl.seq, lval = 0;
+        auto load_lens = [&](int first) {
+            lbase = first;
+            const int ii = first + lane;
+            lval = ii < p.B ? clamp_len(__ldg(p.seq_lens + ii), maxL) : 0;
+        };
+        auto len_of = [&](int ii) -> int {     // warp-uniform
+            if (ii >= p.B) return 0;
+            if (ii - lbase >= 32) load_lens(ii);
+            return __shfl_sync(0xffffffffu, lval, ii - lbase);
+        };
+        auto load_win = [&](int seq, int wb, int nblk) -> int {
+            const int idx = wb + lane;
+            return (seq < p.B && idx < nblk) ? __ldg(p.block_tables + static_cast<size_t>(seq) * p.MB + idx) : -1;
+        };
+        load_lens(pl.seq);
         int i = pl.seq, Si = pl.S, Ui = pl.U;
-        int L = clamp_len(p.seq_lens[i], maxL);
+        int L = len_of(i);
         int n16 = cdiv_i(L, CHUNK), nbl = cdiv_i(L, p.bs);
         int j = pl.cs - Si;
-        int wbase = INT_MIN / 2, wval = -1;
         const int nb = p.bs >= CHUNK ? 1 : CHUNK / p.bs;      // boxes per chunk
+        int wbase = (j * CHUNK) / p.bs;                        // current window: blocks [wbase, wbase+32) of i
+        int wval = load_win(i, wbase, nbl);
+        int nseq = 0, nbase = 0, nval = -1;                    // its successor
+        auto prefetch_next = [&]() {
+            if (wbase + 32 < nbl) {
+                nseq = i; nbase = wbase + 32; nval = load_win(i, nbase, nbl);
+            } else {
+                nseq = i + 1; nbase = 0; nval = load_win(i + 1, 0, cdiv_i(len_of(i + 1), p.bs));
+            }
+        };
+        prefetch_next();
         const int hq0 = hg * p.HPC * p.G;
         int issued = 0, qcount = 0;
         bool ok = true;
         for (int k = pl.cs; k < pl.ce; ++k) {
             while (j >= n16) {
                 Si += n16; Ui += n_units(L, p.P16); ++i;
-                L = clamp_len(p.seq_lens[i], maxL);
-                n16 = cdiv_i(L, CHUNK); nbl = cdiv_i(L, p.bs); j = 0; wbase = INT_MIN / 2;
+                L = len_of(i);
+                n16 = cdiv_i(L, CHUNK); nbl = cdiv_i(L, p.bs); j = 0;
+                wbase = 0;
+                wval = (nseq == i && nbase == 0) ? nval : load_win(i, 0, nbl);
+                prefetch_next();
             }
             const int tok0 = j * CHUNK;
             const int b0 = tok0 / p.bs;
-            if (b0 < wbase || b0 + nb - 1 >= wbase + 32) {
-                wbase = b0;
-                const int idx = wbase + lane;
-                wval = idx < nbl ? __ldg(p.block_tables + static_cast<size_t>(i) * p.MB + idx) : -1;
+            if (b0 + nb - 1 >= wbase + 32) {                   // step to the successor window
+                if (nseq == i && nbase <= b0 && b0 + nb - 1 < nbase + 32) {
+                    wbase = nbase; wval = nval;
+                } else {
+                    wbase = b0; wval = load_win(i, wbase, nbl);
+                }
+                prefetch_next();
             }
             int blk[2];
             blk[0] = __shfl_sync(0xffffffffu, wval, b0 - wbase);
@@ -333,7 +382,9 @@ struct DecodeKernel {
                     if (seg_start) {
                         const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
                             (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
-                        bulk_load(base + p.q_off + qs * p.q_slot_bytes, qsrc, p.q_bytes, &full[slot]);
+                        uint8_t* qdst = base + p.q_off + qs * p.q_slot_bytes;
+                        if (p.q_tma) tma_load_3d(qdst, tq, &full[slot], 0, i * p.Hq + hq0, 0);
+                        else bulk_load(qdst, qsrc, p.q_bytes, &full[slot]);
                         ++qcount;
                     }
                 }
@@ -360,6 +411,16 @@ struct DecodeKernel {
     static __device__ __forceinline__ void store_pair(OutT* dst, float a, float b) {
         dst[0] = from_float<OutT>(a);
         dst[1] = from_float<OutT>(b);
+    }
+
+    // Two query elements (one 32-bit word of QT) as an f16x2 MMA operand.
+    static __device__ __forceinline__ uint32_t to_f16x2(uint32_t w) {
+        if constexpr (QT::code == PA_F16) {
+            return w;
+        } else {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+            return pack2(f.x, f.y, false);
+        }
     }
 
     // Column of accumulator element (tile nt, column pair index within the
@@ -405,25 +466,22 @@ struct DecodeKernel {
             uint8_t* kbuf = base + slot * p.stage_bytes;
             uint8_t* vbuf = kbuf + p.kv_bytes;
             if (d.flags & SEG_START) {
-                load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo, rows_valid, lane);
+                load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo, rows_valid, lane,
+                             p.q_tma, p.HPC * p.G);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&qempty[d.qslot]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
                 m0 = m1 = -INFINITY; l0 = l1 = 0.f;
             }
-            bool wrote = false;
-            if (d.vmask != 0xffffu) {     // zero masked V rows of this head (pool garbage may be NaN)
-                for (int idx = lane; idx < CHUNK * CPR; idx += 32) {
-                    const int tok = idx / CPR, c = idx - tok * CPR;
-                    if (!((d.vmask >> tok) & 1u)) {
-                        const uint32_t a = lay.chunk_addr(lay.row_base(tok, hl), tok, c);
-                        *reinterpret_cast<uint4*>(vbuf + a) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                wrote = true;
-                __syncwarp();
-            }
+            // V fragments of masked token rows are zeroed in registers: the
+            // pool may hold NaN there and 0 * NaN would poison the sum.  A
+            // fragment register holds token 2t in its low half and 2t+1 in
+            // its high half (rows 8+2t, 8+2t+1 for the second k-half).
+            const uint32_t vk0 = (((d.vmask >> (2 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                 (((d.vmask >> (2 * t4 + 1)) & 1u) ? 0xffff0000u : 0u);
+            const uint32_t vk1 = (((d.vmask >> (8 + 2 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                 (((d.vmask >> (9 + 2 * t4)) & 1u) ? 0xffff0000u : 0u);
             // ---- S = Q K^T (16 rows x 16 tokens) ----
             float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             const uint32_t kb = smem_u32(kbuf);
@@ -509,102 +567,120 @@ struct DecodeKernel {
                 for (int j2 = 0; j2 < NT / 2; ++j2) {
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, 2 * j2 + (mi >> 1)), b0, b1, b2, b3);
-                    mma_16816<MMA_BF16>(acc[2 * j2], pa, b0, b1);
-                    mma_16816<MMA_BF16>(acc[2 * j2 + 1], pa, b2, b3);
+                    mma_16816<MMA_BF16>(acc[2 * j2], pa, b0 & vk0, b1 & vk1);
+                    mma_16816<MMA_BF16>(acc[2 * j2 + 1], pa, b2 & vk0, b3 & vk1);
                 }
             } else {
 #pragma unroll
                 for (int c2 = 0; c2 < D / 16; c2 += 2) {
                     uint32_t r0, r1, r2, r3;  // (tok0-7,c) (tok8-15,c) (tok0-7,c+1) (tok8-15,c+1)
                     ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, c2 + (mi >> 1)), r0, r1, r2, r3);
-                    const uint32_t x0 = __byte_perm(r0, 0, 0x3120), x1 = __byte_perm(r1, 0, 0x3120);
-                    const uint32_t x2 = __byte_perm(r2, 0, 0x3120), x3 = __byte_perm(r3, 0, 0x3120);
+                    const uint32_t x0 = __byte_perm(r0 & vk0, 0, 0x3120), x1 = __byte_perm(r1 & vk1, 0, 0x3120);
+                    const uint32_t x2 = __byte_perm(r2 & vk0, 0, 0x3120), x3 = __byte_perm(r3 & vk1, 0, 0x3120);
                     mma_16816<false>(acc[2 * c2], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
                     mma_16816<false>(acc[2 * c2 + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
                     mma_16816<false>(acc[2 * c2 + 2], pa, e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x3));
                     mma_16816<false>(acc[2 * c2 + 3], pa, e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16));
                 }
             }
+            // The stage's shared memory is no longer read: hand it back to
+            // the producer before the segment-end epilogue.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
             if (d.flags & SEG_END) {
                 float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
                 lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
                 float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
                 lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-                const bool v0 = g4 < rows_valid, v1 = g4 + 8 < rows_valid;
-                if (d.flags & DIRECT) {
-                    QE* o = static_cast<QE*>(p.out) + static_cast<size_t>(d.seq) * p.Hq * D;
-                    const float i0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
-                    const float i1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
+                const bool direct = (d.flags & DIRECT) != 0;
+                if (direct || d.slot < p.max_slots) {
+                    float sc0 = p.v_scale, sc1 = p.v_scale;
+                    if (direct) {
+                        sc0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
+                        sc1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
+                    }
+                    QE* orow = static_cast<QE*>(p.out) + (static_cast<size_t>(d.seq) * p.Hq + out_h0) * D;
+                    float* prow = p.part_acc + (static_cast<size_t>(d.slot) * p.Hq + out_h0) * D;
+                    // Each lane stores 4 consecutive columns of a row per pair
+                    // of column tiles.  With fp8 the permuted head_dim order
+                    // already gives every lane 4 consecutive columns; otherwise
+                    // one exchange between lane pairs of a quad assembles them.
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int c0 = out_col(nt, 2 * t4), c1 = out_col(nt, 2 * t4 + 1);
-                        if (v0) {
-                            QE* r = o + static_cast<size_t>(out_h0 + g4) * D;
-                            r[c0] = from_float<QE>(acc[nt][0] * i0);
-                            r[c1] = from_float<QE>(acc[nt][1] * i0);
-                        }
-                        if (v1) {
-                            QE* r = o + static_cast<size_t>(out_h0 + g4 + 8) * D;
-                            r[c0] = from_float<QE>(acc[nt][2] * i1);
-                            r[c1] = from_float<QE>(acc[nt][3] * i1);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh == 1 && rows_valid <= 8) break;      // rows 8..15 are padding
+                        const int row = g4 + 8 * hh;
+                        const float sc = hh ? sc1 : sc0;
+#pragma unroll
+                        for (int q2 = 0; q2 < NT / 2; ++q2) {
+                            const float a0 = acc[2 * q2][2 * hh] * sc, a1 = acc[2 * q2][2 * hh + 1] * sc;
+                            const float b0 = acc[2 * q2 + 1][2 * hh] * sc, b1 = acc[2 * q2 + 1][2 * hh + 1] * sc;
+                            float v[4];
+                            int col;
+                            if constexpr (FP8) {
+                                v[0] = a0; v[1] = b0; v[2] = a1; v[3] = b1;
+                                col = 16 * q2 + 4 * t4;
+                            } else {
+                                const bool odd = (t4 & 1) != 0;
+                                const float r0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
+                                const float r1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
+                                if (odd) { v[0] = r0; v[1] = r1; v[2] = b0; v[3] = b1; col = 16 * q2 + 8 + 2 * (t4 - 1); }
+                                else     { v[0] = a0; v[1] = a1; v[2] = r0; v[3] = r1; col = 16 * q2 + 2 * t4; }
+                            }
+                            if (row < rows_valid) {
+                                if (direct) store4<QE>(orow + static_cast<size_t>(row) * D + col, v);
+                                else store4<float>(prow + static_cast<size_t>(row) * D + col, v);
+                            }
                         }
                     }
-                } else if (d.slot < p.max_slots) {
-                    float* pa_ = p.part_acc + static_cast<size_t>(d.slot) * p.Hq * D;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int c0 = out_col(nt, 2 * t4), c1 = out_col(nt, 2 * t4 + 1);
-                        if (v0) {
-                            float* r = pa_ + static_cast<size_t>(out_h0 + g4) * D;
-                            r[c0] = acc[nt][0] * p.v_scale;
-                            r[c1] = acc[nt][1] * p.v_scale;
-                        }
-                        if (v1) {
-                            float* r = pa_ + static_cast<size_t>(out_h0 + g4 + 8) * D;
-                            r[c0] = acc[nt][2] * p.v_scale;
-                            r[c1] = acc[nt][3] * p.v_scale;
-                        }
-                    }
-                    if (t4 == 0) {
+                    if (!direct && t4 == 0) {
                         float2* ml = p.part_ml + static_cast<size_t>(d.slot) * p.Hq;
-                        if (v0) ml[out_h0 + g4] = make_float2(m0, lt0);
-                        if (v1) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
+                        if (g4 < rows_valid) ml[out_h0 + g4] = make_float2(m0, lt0);
+                        if (g4 + 8 < rows_valid) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
                     }
                 }
             }
-            if (wrote) fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
         }
     }
 
     // A fragments of this tile's query rows (16 x D) from the stage's query
     // copy; rows past the group are zero.
     static __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[KS][4], const uint8_t* qbuf,
-                                                        int qrow_lo, int rows_valid, int lane) {
+                                                        int qrow_lo, int rows_valid, int lane,
+                                                        int q_tma, int qrows) {
         const int g4 = lane >> 2, t4 = lane & 3;
+        // byte offset of 16-byte column chunk c of query row r in the ring
+        // slot: [column block][row][128 B] with the 128-B swizzle when the
+        // rows came by tensor copy, plain row-major otherwise
+        auto qaddr = [&](int r, int c) -> uint32_t {
+            if (q_tma) {
+                const int rr = (c >> 3) * qrows + r;
+                return static_cast<uint32_t>(rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
+            }
+            return static_cast<uint32_t>(r * D * 2 + c * 16);
+        };
         if constexpr (!FP8) {
             const int mi = lane >> 3, r8 = lane & 7;
             int row = (mi & 1) * 8 + r8;
             if (row >= rows_valid) row = 0;
-            const uint32_t rb = smem_u32(qbuf) + static_cast<uint32_t>((qrow_lo + row) * D * 2);
+            const uint32_t qb = smem_u32(qbuf);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                ldsm_x4(rb + (2 * ks + (mi >> 1)) * 16, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+                ldsm_x4(qb + qaddr(qrow_lo + row, 2 * ks + (mi >> 1)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
             }
         } else {
             // head_dim order inside a 16-wide k-step is permuted to match the
             // byte order of e4m3 key rows: logical k (2t, 2t+1, 2t+8, 2t+9)
             // holds physical dims (4t, 4t+1, 4t+2, 4t+3).
-            const QE* q0 = reinterpret_cast<const QE*>(qbuf) + static_cast<size_t>(qrow_lo + min(g4, rows_valid - 1)) * D;
-            const QE* q1 = reinterpret_cast<const QE*>(qbuf) + static_cast<size_t>(qrow_lo + min(g4 + 8, rows_valid - 1)) * D;
+            const int r0 = qrow_lo + min(g4, rows_valid - 1), r1 = qrow_lo + min(g4 + 8, rows_valid - 1);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const int d0 = 16 * ks + 4 * t4;
-                qa[ks][0] = pack2(to_float(q0[d0]), to_float(q0[d0 + 1]), false);
-                qa[ks][1] = pack2(to_float(q1[d0]), to_float(q1[d0 + 1]), false);
-                qa[ks][2] = pack2(to_float(q0[d0 + 2]), to_float(q0[d0 + 3]), false);
-                qa[ks][3] = pack2(to_float(q1[d0 + 2]), to_float(q1[d0 + 3]), false);
+                const int c = 2 * ks + (t4 >> 1), inner = 8 * (t4 & 1);
+                const uint2 u0 = *reinterpret_cast<const uint2*>(qbuf + qaddr(r0, c) + inner);
+                const uint2 u1 = *reinterpret_cast<const uint2*>(qbuf + qaddr(r1, c) + inner);
+                qa[ks][0] = to_f16x2(u0.x);
+                qa[ks][1] = to_f16x2(u1.x);
+                qa[ks][2] = to_f16x2(u0.y);
+                qa[ks][3] = to_f16x2(u1.y);
             }
         }
         if (g4 >= rows_valid) {
@@ -806,7 +882,7 @@ struct DecodeKernel {
 template <class KV, class QT, int D, bool TC>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
-                 const __grid_constant__ CUtensorMap tv) {
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
     using K = DecodeKernel<KV, QT, D, TC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -822,7 +898,6 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     const int range = blockIdx.x / p.NHG;
     Plan pl;
     make_plan(p, range, scratch, s_first, s_tot, pl);
-    grid_dependents_launch();     // the reduce kernel may start its own prologue
     if (pl.cs >= pl.ce || pl.seq < 0) return;
 
     const int warp = threadIdx.x >> 5;
@@ -837,8 +912,12 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     }
     __syncthreads();
     if (warp == p.NCW) {
-        if ((threadIdx.x & 31) == 0) { prefetch_tensormap(&tk); prefetch_tensormap(&tv); }
-        K::producer(p, pl, hg, base, full, empty, qempty, descs, &tk, &tv);
+        if ((threadIdx.x & 31) == 0) {
+            prefetch_tensormap(&tk);
+            prefetch_tensormap(&tv);
+            if (p.q_tma) prefetch_tensormap(&tq);
+        }
+        K::producer(p, pl, hg, base, full, empty, qempty, descs, &tk, &tv, &tq);
     } else if (warp < p.NCW) {
         if constexpr (TC) {
             K::consumer_tc(p, pl, hg, warp, base, full, empty, qempty, descs);
