@@ -97,16 +97,27 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
  *   s_t   = scale * <q[i,h,:], K_t>            t in [0, L)
  *   out   = sum_t softmax(s)_t * V_t
  * where K_t, V_t are row (t % block_size, g) of physical block
- * block_tables[i][t / block_size].  fp8 caches are dequantised in registers:
- * K_t = e4m3(k) * k_scale, V_t = e4m3(v) * v_scale (scales ignored otherwise).
+ * block_tables[i][t / block_size].  fp8 caches are read as
+ * K_t = e4m3(k) * k_scale, V_t = e4m3(v) * v_scale (scales ignored otherwise);
+ * the scales are applied to the scores and the output, never per element.
  * L == 0 writes zeros.
  *
- * The work is split into 16-token chunks, balanced over persistent CTAs;
- * sequences spanning several CTAs (or longer than partition_tokens) are
- * merged afterwards by a log-sum-exp reduction kernel on the same stream.
+ * The work is split into chunks of 16 tokens (32 for fp8 caches with
+ * head_dim 128 and at most 8 query heads per KV head), balanced over
+ * persistent CTAs; sequences spanning several CTAs (or longer than
+ * partition_tokens) are merged afterwards by a log-sum-exp reduction kernel
+ * on the same stream.
  *   partition_tokens  0 lets the library choose split points; otherwise a
  *                     positive multiple of 16: sequences are additionally
  *                     split every partition_tokens tokens.
+ * Precision: scores and sums accumulate in fp32.  The probabilities enter
+ * P*V rounded to the MMA operand type: bf16 (8 significant bits) for bf16
+ * caches, f16 (11 bits) for f16 caches and fp8 caches on 16-token chunks.
+ * On the fp8 32-token path the query and the probabilities are each carried
+ * as two e4m3 terms, 8 significant bits (exact for bf16 queries, except
+ * elements below 2^-9 of the largest in their GQA group); an infinite query
+ * element saturates to +-448 there instead of propagating.  pa_decode_simt
+ * keeps everything in fp32.
  *   workspace         device buffer of at least pa_decode_workspace_size(...)
  *                     bytes, 256-byte aligned; contents need no initialisation
  *                     and are scratch between calls.  Calls sharing one

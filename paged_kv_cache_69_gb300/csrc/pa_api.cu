@@ -172,7 +172,15 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     }
     if (tc && kv_dtype == PA_F32)
         return fail(PA_ERR_UNSUPPORTED, "decode: f32 caches run on the CUDA-core path (pa_decode_simt)");
-    const void* kern = tc ? decode_kernel_tc(kv_dtype, q_dtype, D) : decode_kernel_simt(kv_dtype, q_dtype, D);
+    // fp8 caches on the tensor-core path run the native-e4m3 kernel (32-token
+    // chunks, GQA groups of up to 8 heads, partitions a multiple of 32
+    // tokens); other fp8 shapes convert e4m3 to f16 in registers.
+    const bool native8 = tc && kv_dtype == PA_FP8_E4M3 && D == 128 && Hq / Hkv <= 8 &&
+                         partition_tokens % 32 == 0;
+    const int CT = native8 ? 32 : 16;
+    const void* kern = native8 ? decode_kernel_e4m3(q_dtype, D)
+                       : tc    ? decode_kernel_tc(kv_dtype, q_dtype, D)
+                               : decode_kernel_simt(kv_dtype, q_dtype, D);
     if (!kern) return fail(PA_ERR_UNSUPPORTED, "decode: no kernel for this dtype / head_dim combination");
     const void* rkern = reduce_kernel(q_dtype, D);
     if (!rkern) return fail(PA_ERR_UNSUPPORTED, "decode: no reduce kernel for this output dtype");
@@ -188,14 +196,14 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     for (int h = Hkv; h >= 1; --h) {
         if (Hkv % h) continue;
         if (h * MT > 8) continue;
-        if (16LL * h * D * e > 32 * 1024) continue;
+        if (static_cast<long long>(CT) * h * D * e > 32 * 1024) continue;
         HPC = h;
         break;
     }
     if (HPC == 0) return fail(PA_ERR_UNSUPPORTED, "decode: no head grouping fits one CTA");
     const int NHG = Hkv / HPC;
     const int NCW = HPC * MT;
-    const int rpb = std::min(16, bs);
+    const int rpb = std::min(CT, bs);
     const int DH = D * e / 128;
     if (DH < 1 || (D * e) % 128 != 0) return fail(PA_ERR_UNSUPPORTED, "decode: head_dim * elem bytes must be a multiple of 128");
 
@@ -204,10 +212,11 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.D = D; p.bs = bs; p.NB = NB; p.MB = MB;
     p.out_bytes = eq;
     p.HPC = HPC; p.NHG = NHG; p.MT = MT; p.NCW = NCW;
-    p.P16 = partition_tokens / 16;
+    p.ct = CT;
+    p.PC = partition_tokens / CT;
     p.rpb = rpb;
     p.box_bytes = static_cast<uint32_t>(rpb * HPC * DH * 128);
-    p.kv_bytes = static_cast<uint32_t>(16 * HPC * D * e);
+    p.kv_bytes = static_cast<uint32_t>(CT * HPC * D * e);
     p.q_bytes = static_cast<uint32_t>(HPC * G * D * eq);
     p.q_slot_bytes = (p.q_bytes + 1023u) & ~1023u;   // swizzled tensor copies need 1024-B alignment
     p.stage_bytes = 2 * p.kv_bytes;
@@ -234,7 +243,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         const long long per_cta = std::min(dev.max_smem, 227 * 1024) - static_cast<long long>(fixed);
         stages = static_cast<int>(std::min<long long>(MAX_STAGES, per_cta / p.stage_bytes));
         // roughly 160 KB of K/V in flight per CTA; more stages buy nothing
-        stages = std::min(stages, std::max(2, static_cast<int>((160 * 1024) / p.stage_bytes)));
+        const int want = native8 ? cdiv_h(160 * 1024, p.stage_bytes) : static_cast<int>((160 * 1024) / p.stage_bytes);
+        stages = std::min(stages, std::max(2, want));
     }
     if (stages < 2) return fail(PA_ERR_UNSUPPORTED, "decode: pipeline stages do not fit in shared memory");
     p.stages = stages;
@@ -301,7 +311,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (ce != cudaSuccess) return fail_cuda("decode: occupancy query", ce);
     per_sm = std::max(1, per_sm);
-    const long long chunk_bound = static_cast<long long>(B) * cdiv_h(static_cast<long long>(MB) * bs, 16);
+    const long long chunk_bound = static_cast<long long>(B) * cdiv_h(static_cast<long long>(MB) * bs, CT);
     long long NR = std::max(1LL, static_cast<long long>(per_sm) * dev.sms / NHG);
     NR = std::min(NR, 2LL * dev.sms);   // the workspace holds 2 x SMs ranges
     NR = std::min(NR, chunk_bound);

@@ -1,0 +1,18 @@
+// pa_decode_e4m3.cu -- native-e4m3 tensor-core instantiations of the paged
+// decode kernel (fp8 caches, head_dim 128, 32-token chunks, mma.sync
+// m16n8k32 with e4m3 operands and fp32 accumulation).
+#include <cuda.h>
+
+#include "pa_decode_kernel.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+const void* decode_kernel_e4m3(pa_dtype q, int D) {
+    if (D != 128) return nullptr;
+    if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, true, 32>);
+    if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, true, 32>);
+    return nullptr;
+}
+
+}  // namespace pa

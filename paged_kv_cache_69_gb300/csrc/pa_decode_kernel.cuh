@@ -30,12 +30,12 @@
 
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "pa_device.cuh"
 
 namespace pa {
 
-constexpr int CHUNK = 16;            // tokens per pipeline stage
 constexpr int MAX_STAGES = 8;
 constexpr int NQ = 2;                // query-row ring slots
 constexpr int MAX_WARPS = 9;         // up to 8 consumers + 1 producer
@@ -65,7 +65,8 @@ struct DecodeParams {
     int B, Hq, Hkv, G, D, bs, NB, MB;
     int out_bytes;            // bytes of one output element
     int HPC, NHG, NR, MT, NCW;
-    int P16;                  // partition length in chunks, 0 = none
+    int ct;                   // tokens per chunk (pipeline stage): 16, or 32 for native e4m3
+    int PC;                   // partition length in chunks, 0 = none
     int max_slots;
     float qk_scale;           // scale * log2(e) (* k_scale for fp8)
     float v_scale;            // v_scale for fp8, else 1
@@ -88,9 +89,9 @@ __device__ __forceinline__ int cdiv_i(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ int clamp_len(int L, int maxL) {
     return L < 0 ? 0 : (L > maxL ? maxL : L);
 }
-__device__ __forceinline__ int n_units(int L, int P16) {
-    const int n16 = cdiv_i(L, CHUNK);
-    return n16 == 0 ? 0 : (P16 > 0 ? cdiv_i(n16, P16) : 1);
+__device__ __forceinline__ int n_units(int L, int PC, int ct) {
+    const int nch = cdiv_i(L, ct);
+    return nch == 0 ? 0 : (PC > 0 ? cdiv_i(nch, PC) : 1);
 }
 // The range (CTA column) owning global chunk c: largest r with
 // floor(r * C / NR) <= c.
@@ -141,8 +142,8 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
         const int Lraw = p.seq_lens[i];
         bad |= (Lraw < 0 || Lraw > maxL);
         const int L = clamp_len(Lraw, maxL);
-        csum += cdiv_i(L, CHUNK);
-        usum += n_units(L, p.P16);
+        csum += cdiv_i(L, p.ct);
+        usum += n_units(L, p.PC, p.ct);
     }
     if (bad && blockIdx.x == 0) raise_flag(p.err_flag, PA_ERRBIT_SEQ_TOO_LONG);
     if (blockIdx.x == 0 && tid == 0) p.totals[2] = 0;
@@ -168,10 +169,10 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
         int S = cpre, U = upre;
         for (int i = i0; i < i1; ++i) {
             const int L = clamp_len(p.seq_lens[i], maxL);
-            const int n16 = cdiv_i(L, CHUNK);
-            if (cs < S + n16) { *s_first = make_int4(i, S, U, 0); break; }
-            S += n16;
-            U += n_units(L, p.P16);
+            const int nch = cdiv_i(L, p.ct);
+            if (cs < S + nch) { *s_first = make_int4(i, S, U, 0); break; }
+            S += nch;
+            U += n_units(L, p.PC, p.ct);
         }
     }
     if (blockIdx.x == 0) {
@@ -180,15 +181,15 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
         int S = cpre, U = upre;
         for (int i = i0; i < i1; ++i) {
             const int L = clamp_len(p.seq_lens[i], maxL);
-            const int n16 = cdiv_i(L, CHUNK), nu = n_units(L, p.P16);
+            const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
             if (L == 0) {
                 uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
                                                     static_cast<size_t>(i) * p.Hq * p.D * p.out_bytes);
                 for (int k = 0; k < p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
-            } else if (!(nu == 1 && range_of(S, C, p.NR) == range_of(S + n16 - 1, C, p.NR))) {
+            } else if (!(nu == 1 && range_of(S, C, p.NR) == range_of(S + nch - 1, C, p.NR))) {
                 p.split_list[atomicAdd(&p.totals[2], 1)] = make_int4(i, S, U, L);
             }
-            S += n16;
+            S += nch;
             U += nu;
         }
         if (tid == 0) { p.totals[0] = C; p.totals[1] = Ut; }
@@ -232,11 +233,16 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16*
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v[0], v[1], true), pack2(v[2], v[3], true));
 }
 
-template <class KV, class QT, int D, bool TC>
+template <class KV, class QT, int D, bool TC, int CT>
 struct DecodeKernel {
     using KT = typename KV::T;
     using QE = typename QT::T;
     static constexpr bool FP8 = (KV::code == PA_FP8_E4M3);
+    // 32-token chunks are the native-e4m3 tensor-core variant (fp8 operands,
+    // m16n8k32); every other variant runs 16-token chunks.
+    static constexpr bool NATIVE8 = (CT == 32);
+    static_assert(CT == 16 || (CT == 32 && FP8 && TC && D == 128), "32-token chunks: fp8 tensor-core path only");
+    static constexpr int MAXB = CT / 8;       // TMA boxes per chunk at the smallest block size
     static constexpr bool MMA_BF16 = (KV::code == PA_BF16);   // fp8 runs in f16
     static constexpr int NT = D / 8;          // 8-wide output column tiles
     static constexpr int KS = D / 16;         // 16-deep k-steps over head_dim
@@ -272,10 +278,10 @@ struct DecodeKernel {
         load_lens(pl.seq);
         int i = pl.seq, Si = pl.S, Ui = pl.U;
         int L = len_of(i);
-        int n16 = cdiv_i(L, CHUNK), nbl = cdiv_i(L, p.bs);
+        int nch = cdiv_i(L, CT), nbl = cdiv_i(L, p.bs);
         int j = pl.cs - Si;
-        const int nb = p.bs >= CHUNK ? 1 : CHUNK / p.bs;      // boxes per chunk
-        int wbase = (j * CHUNK) / p.bs;                        // current window: blocks [wbase, wbase+32) of i
+        const int nb = p.bs >= CT ? 1 : CT / p.bs;      // boxes per chunk
+        int wbase = (j * CT) / p.bs;                        // current window: blocks [wbase, wbase+32) of i
         int wval = load_win(i, wbase, nbl);
         int nseq = 0, nbase = 0, nval = -1;                    // its successor
         auto prefetch_next = [&]() {
@@ -290,15 +296,15 @@ struct DecodeKernel {
         int issued = 0, qcount = 0;
         bool ok = true;
         for (int k = pl.cs; k < pl.ce; ++k) {
-            while (j >= n16) {
-                Si += n16; Ui += n_units(L, p.P16); ++i;
+            while (j >= nch) {
+                Si += nch; Ui += n_units(L, p.PC, p.ct); ++i;
                 L = len_of(i);
-                n16 = cdiv_i(L, CHUNK); nbl = cdiv_i(L, p.bs); j = 0;
+                nch = cdiv_i(L, CT); nbl = cdiv_i(L, p.bs); j = 0;
                 wbase = 0;
                 wval = (nseq == i && nbase == 0) ? nval : load_win(i, 0, nbl);
                 prefetch_next();
             }
-            const int tok0 = j * CHUNK;
+            const int tok0 = j * CT;
             const int b0 = tok0 / p.bs;
             if (b0 + nb - 1 >= wbase + 32) {                   // step to the successor window
                 if (nseq == i && nbase <= b0 && b0 + nb - 1 < nbase + 32) {
@@ -308,9 +314,9 @@ struct DecodeKernel {
                 }
                 prefetch_next();
             }
-            int blk[2];
-            blk[0] = __shfl_sync(0xffffffffu, wval, b0 - wbase);
-            blk[1] = __shfl_sync(0xffffffffu, wval, min(b0 + 1 - wbase, 31));
+            int blk[MAXB];
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) blk[b] = __shfl_sync(0xffffffffu, wval, min(b0 + b - wbase, 31));
             if (lane == 0) {
                 const int slot = issued % S;
                 const uint32_t round = issued / S;
@@ -318,7 +324,7 @@ struct DecodeKernel {
                     raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
                     ok = false;
                 }
-                const bool seg_start = (k == pl.cs) || (j == 0) || (p.P16 > 0 && j % p.P16 == 0);
+                const bool seg_start = (k == pl.cs) || (j == 0) || (p.PC > 0 && j % p.PC == 0);
                 const int qs = qcount % NQ;
                 if (ok && seg_start && qcount >= NQ &&
                     !mbar_wait_bounded(&qempty[qs], ((qcount / NQ) - 1) & 1u)) {
@@ -326,18 +332,21 @@ struct DecodeKernel {
                     ok = false;
                 }
                 if (ok) {
-                    const int ntok = min(CHUNK, L - tok0);
+                    const int ntok = min(CT, L - tok0);
+                    const uint32_t vmask_full = CT == 32 ? 0xffffffffu : ((1u << CT) - 1u);
                     uint32_t vmask = (ntok >= 32) ? 0xffffffffu : ((1u << ntok) - 1u);
-                    vmask &= 0xffffu;
+                    vmask &= vmask_full;
                     uint32_t nbox_issued = 0;
                     uint8_t* kbuf = base + slot * p.stage_bytes;
                     uint8_t* vbuf = kbuf + p.kv_bytes;
                     uint32_t issue_mask = 0;
-                    for (int b = 0; b < nb; ++b) {
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b) {
+                        if (b >= nb) break;
                         const int first = b * p.rpb;
                         if (first >= ntok) continue;                 // nothing valid here
                         const int id = blk[b];
-                        const uint32_t rows = ((1u << p.rpb) - 1u) << first;
+                        const uint32_t rows = (p.rpb >= 32 ? 0xffffffffu : ((1u << p.rpb) - 1u)) << first;
                         if (id < 0 || id >= p.NB) {
                             raise_flag(p.err_flag, PA_ERRBIT_BAD_BLOCK);
                             vmask &= ~rows;
@@ -347,22 +356,24 @@ struct DecodeKernel {
                         ++nbox_issued;
                     }
                     uint32_t flags = 0;
-                    const bool seg_end = (k == pl.ce - 1) || (j == n16 - 1) ||
-                                         (p.P16 > 0 && (j + 1) % p.P16 == 0);
+                    const bool seg_end = (k == pl.ce - 1) || (j == nch - 1) ||
+                                         (p.PC > 0 && (j + 1) % p.PC == 0);
                     if (seg_start) flags |= SEG_START;
                     if (seg_end) flags |= SEG_END;
-                    const int nu = n_units(L, p.P16);
-                    if (nu == 1 && Si >= pl.cs && Si + n16 <= pl.ce) flags |= DIRECT;
+                    const int nu = n_units(L, p.PC, p.ct);
+                    if (nu == 1 && Si >= pl.cs && Si + nch <= pl.ce) flags |= DIRECT;
                     StageDesc d;
                     d.seq = i; d.tok0 = tok0; d.vmask = vmask; d.flags = flags;
-                    d.slot = (blockIdx.x / p.NHG) + Ui + (p.P16 > 0 ? j / p.P16 : 0);
+                    d.slot = (blockIdx.x / p.NHG) + Ui + (p.PC > 0 ? j / p.PC : 0);
                     d.qslot = qs;
                     descs[slot] = d;
                     const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (seg_start ? p.q_bytes : 0u);
                     mbar_arrive_expect_tx(&full[slot], bytes);
-                    for (int b = 0; b < nb; ++b) {
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b) {
+                        if (b >= nb) break;
                         if (!((issue_mask >> b) & 1u)) continue;
-                        const int row0 = blk[b] * p.bs + (p.bs > CHUNK ? (tok0 % p.bs) : 0);
+                        const int row0 = blk[b] * p.bs + (p.bs > CT ? (tok0 % p.bs) : 0);
                         uint8_t* kd = kbuf + b * p.box_bytes;
                         uint8_t* vd = vbuf + b * p.box_bytes;
                         if (!p.per_head_copies) {
@@ -430,6 +441,67 @@ struct DecodeKernel {
             return 16 * (nt >> 1) + 2 * n + (nt & 1);
         } else {
             return nt * 8 + n;
+        }
+    }
+
+    // End of a segment: the normalised output rows when the segment covers
+    // the whole sequence (DIRECT), else the unnormalised partial (acc, m, l)
+    // for the merge kernel.  Rows g4 and g4 + 8 of the tile, columns from
+    // out_col().
+    static __device__ __forceinline__ void finish_segment(const DecodeParams& p, const StageDesc& d,
+                                                          const float (&acc)[NT][4], float m0, float m1,
+                                                          float l0, float l1, int lane, int rows_valid,
+                                                          int out_h0) {
+        const int g4 = lane >> 2, t4 = lane & 3;
+        float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+        float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+        const bool direct = (d.flags & DIRECT) != 0;
+        if (direct || d.slot < p.max_slots) {
+            float sc0 = p.v_scale, sc1 = p.v_scale;
+            if (direct) {
+                sc0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
+                sc1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
+            }
+            QE* orow = static_cast<QE*>(p.out) + (static_cast<size_t>(d.seq) * p.Hq + out_h0) * D;
+            float* prow = p.part_acc + (static_cast<size_t>(d.slot) * p.Hq + out_h0) * D;
+            // Each lane stores 4 consecutive columns of a row per pair
+            // of column tiles.  With fp8 the permuted head_dim order
+            // already gives every lane 4 consecutive columns; otherwise
+            // one exchange between lane pairs of a quad assembles them.
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh == 1 && rows_valid <= 8) break;      // rows 8..15 are padding
+                const int row = g4 + 8 * hh;
+                const float sc = hh ? sc1 : sc0;
+#pragma unroll
+                for (int q2 = 0; q2 < NT / 2; ++q2) {
+                    const float a0 = acc[2 * q2][2 * hh] * sc, a1 = acc[2 * q2][2 * hh + 1] * sc;
+                    const float b0 = acc[2 * q2 + 1][2 * hh] * sc, b1 = acc[2 * q2 + 1][2 * hh + 1] * sc;
+                    float v[4];
+                    int col;
+                    if constexpr (FP8) {
+                        v[0] = a0; v[1] = b0; v[2] = a1; v[3] = b1;
+                        col = 16 * q2 + 4 * t4;
+                    } else {
+                        const bool odd = (t4 & 1) != 0;
+                        const float r0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
+                        const float r1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
+                        if (odd) { v[0] = r0; v[1] = r1; v[2] = b0; v[3] = b1; col = 16 * q2 + 8 + 2 * (t4 - 1); }
+                        else     { v[0] = a0; v[1] = a1; v[2] = r0; v[3] = r1; col = 16 * q2 + 2 * t4; }
+                    }
+                    if (row < rows_valid) {
+                        if (direct) store4<QE>(orow + static_cast<size_t>(row) * D + col, v);
+                        else store4<float>(prow + static_cast<size_t>(row) * D + col, v);
+                    }
+                }
+            }
+            if (!direct && t4 == 0) {
+                float2* ml = p.part_ml + static_cast<size_t>(d.slot) * p.Hq;
+                if (g4 < rows_valid) ml[out_h0 + g4] = make_float2(m0, lt0);
+                if (g4 + 8 < rows_valid) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
+            }
         }
     }
 
@@ -587,59 +659,249 @@ struct DecodeKernel {
             // the producer before the segment-end epilogue.
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (d.flags & SEG_END) {
-                float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-                lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
-                float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-                lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-                const bool direct = (d.flags & DIRECT) != 0;
-                if (direct || d.slot < p.max_slots) {
-                    float sc0 = p.v_scale, sc1 = p.v_scale;
-                    if (direct) {
-                        sc0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
-                        sc1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
-                    }
-                    QE* orow = static_cast<QE*>(p.out) + (static_cast<size_t>(d.seq) * p.Hq + out_h0) * D;
-                    float* prow = p.part_acc + (static_cast<size_t>(d.slot) * p.Hq + out_h0) * D;
-                    // Each lane stores 4 consecutive columns of a row per pair
-                    // of column tiles.  With fp8 the permuted head_dim order
-                    // already gives every lane 4 consecutive columns; otherwise
-                    // one exchange between lane pairs of a quad assembles them.
+            if (d.flags & SEG_END) finish_segment(p, d, acc, m0, m1, l0, l1, lane, rows_valid, out_h0);
+        }
+    }
+
+    // ---------------- native-e4m3 tensor-core consumer ----------------
+    // fp8 caches, 32-token chunks, GQA groups of at most 8 query heads.  The
+    // key and value bytes enter the MMA as stored (m16n8k32, e4m3 x e4m3 ->
+    // fp32), so nothing is converted per token.  The query and the softmax
+    // weights are each carried as two e4m3 terms, hi = e4m3(x) and
+    // lo = e4m3(x - hi) (about 8 significant bits together), placed in the
+    // two halves of the 16-row tile: row r < 8 holds the hi term of query
+    // head r and row r + 8 its lo term.  A lane owns rows g and g + 8 of
+    // every accumulator tile, so hi + lo is a register add: scores after
+    // Q K^T, outputs at the end of the segment.  The query tile is scaled by
+    // a power of two 2^e putting its largest magnitude in [128, 256) (2^-e
+    // goes into the score scale), and the weights are 2^8 * exp2(s - m), in
+    // [0, 256]: that factor is common to acc and l and cancels in acc / l
+    // and in the log-sum-exp merge.
+    static constexpr int KS8 = D / 32;        // 32-deep k-steps over head_dim
+
+    static __device__ __forceinline__ uint32_t token_bytemask(uint32_t x) {
+        // bits 0, 1, 8, 9 of x -> bytes 0, 1, 2, 3 (0xff where set)
+        const uint32_t y = (x & 1u) | ((x & 2u) << 7) | ((x & 0x100u) << 8) | ((x & 0x200u) << 15);
+        return y * 0xffu;
+    }
+
+    // (hi, lo) e4m3 byte pairs of two non-negative weights
+    static __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+        const uint32_t h = f32x2_to_f16x2(a, b);
+        hi = f16x2_to_e4m3x2(h);
+        lo = f16x2_to_e4m3x2(sub_f16x2(h, e4m3x2_to_f16x2(hi)));
+    }
+
+    static __device__ void consumer_e4m3(const DecodeParams& p, const Plan& pl, int hg, int w,
+                                         uint8_t* base, uint64_t* full, uint64_t* empty, uint64_t* qempty,
+                                         const StageDesc* descs) {
+        const int lane = threadIdx.x & 31;
+        const int t4 = lane & 3;
+        const int hl = w;                           // one tile per KV head (G <= 8)
+        const int rows_valid = p.G;
+        const int S = p.stages;
+        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
+                           static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
+        const int mi = lane >> 3, r8 = lane & 7;
+        // K: ldmatrix matrices (tokens 0-7, k 0-15 | tokens 0-7, k 16-31 |
+        // tokens 8-15, k 0-15 | tokens 8-15, k 16-31) of each half-chunk
+        const int tokK = (mi >> 1) * 8 + r8;
+        const uint32_t rbK0 = lay.row_base(tokK, hl), rbK1 = lay.row_base(tokK + 16, hl);
+        // V (transposed): matrix mi holds tokens 8mi .. 8mi+7 of a 16-byte column chunk
+        const int tokV = mi * 8 + r8;
+        const uint32_t rbV = lay.row_base(tokV, hl);
+
+        float acc[NT][4];
+        uint32_t qa[KS8][4];
+        float m0 = -INFINITY, l0 = 0.f;
+        float qk_scale = p.qk_scale;
+        const int qrow_lo = hl * p.G;
+        const int out_h0 = hg * p.HPC * p.G + qrow_lo;
+
+        for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
+            const int slot = st % S;
+            if (!mbar_wait_bounded(&full[slot], (st / S) & 1u)) {
+                if (lane == 0) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                return;
+            }
+            const StageDesc d = descs[slot];
+            uint8_t* kbuf = base + slot * p.stage_bytes;
+            uint8_t* vbuf = kbuf + p.kv_bytes;
+            if (d.flags & SEG_START) {
+                qk_scale = p.qk_scale * load_q_e4m3(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo,
+                                                    rows_valid, lane, p.q_tma, p.HPC * p.G);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (hh == 1 && rows_valid <= 8) break;      // rows 8..15 are padding
-                        const int row = g4 + 8 * hh;
-                        const float sc = hh ? sc1 : sc0;
+                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+                m0 = -INFINITY; l0 = 0.f;
+            }
+            // ---- S = Q K^T: 16 rows x 32 tokens, four 8-token tiles ----
+            float s[4][4];
 #pragma unroll
-                        for (int q2 = 0; q2 < NT / 2; ++q2) {
-                            const float a0 = acc[2 * q2][2 * hh] * sc, a1 = acc[2 * q2][2 * hh + 1] * sc;
-                            const float b0 = acc[2 * q2 + 1][2 * hh] * sc, b1 = acc[2 * q2 + 1][2 * hh + 1] * sc;
-                            float v[4];
-                            int col;
-                            if constexpr (FP8) {
-                                v[0] = a0; v[1] = b0; v[2] = a1; v[3] = b1;
-                                col = 16 * q2 + 4 * t4;
-                            } else {
-                                const bool odd = (t4 & 1) != 0;
-                                const float r0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
-                                const float r1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
-                                if (odd) { v[0] = r0; v[1] = r1; v[2] = b0; v[3] = b1; col = 16 * q2 + 8 + 2 * (t4 - 1); }
-                                else     { v[0] = a0; v[1] = a1; v[2] = r0; v[3] = r1; col = 16 * q2 + 2 * t4; }
-                            }
-                            if (row < rows_valid) {
-                                if (direct) store4<QE>(orow + static_cast<size_t>(row) * D + col, v);
-                                else store4<float>(prow + static_cast<size_t>(row) * D + col, v);
-                            }
-                        }
-                    }
-                    if (!direct && t4 == 0) {
-                        float2* ml = p.part_ml + static_cast<size_t>(d.slot) * p.Hq;
-                        if (g4 < rows_valid) ml[out_h0 + g4] = make_float2(m0, lt0);
-                        if (g4 + 8 < rows_valid) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
-                    }
+            for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            const uint32_t kb = smem_u32(kbuf);
+#pragma unroll
+            for (int ks = 0; ks < KS8; ++ks) {
+                uint32_t r0, r1, r2, r3, c0, c1, c2, c3;
+                ldsm_x4(kb + lay.chunk_addr(rbK0, tokK, 2 * ks + (mi & 1)), r0, r1, r2, r3);
+                ldsm_x4(kb + lay.chunk_addr(rbK1, tokK, 2 * ks + (mi & 1)), c0, c1, c2, c3);
+                mma_e4m3_16832(s[0], qa[ks], r0, r1);
+                mma_e4m3_16832(s[1], qa[ks], r2, r3);
+                mma_e4m3_16832(s[2], qa[ks], c0, c1);
+                mma_e4m3_16832(s[3], qa[ks], c2, c3);
+            }
+            // ---- online softmax (log2 domain) of row g4 over 8 tokens per lane ----
+            float x[4][2];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = nt * 8 + 2 * t4 + e;
+                    x[nt][e] = ((d.vmask >> col) & 1u) ? (s[nt][e] + s[nt][e + 2]) * qk_scale : -INFINITY;
+                }
+            float mx = fmaxf(fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1])),
+                             fmaxf(fmaxf(x[2][0], x[2][1]), fmaxf(x[3][0], x[3][1])));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mn = fmaxf(m0, mx);
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            const float al = exp2f(m0 - mu);
+            m0 = mn;
+            const float eb = mu - 8.f;                 // weights scaled by 2^8
+            float pr[4][2];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                pr[nt][0] = exp2f(x[nt][0] - eb);
+                pr[nt][1] = exp2f(x[nt][1] - eb);
+            }
+            l0 = l0 * al + (((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1])) +
+                            ((pr[2][0] + pr[2][1]) + (pr[3][0] + pr[3][1])));
+            if (!__all_sync(0xffffffffu, al == 1.f)) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    acc[nt][0] *= al; acc[nt][1] *= al; acc[nt][2] *= al; acc[nt][3] *= al;
                 }
             }
+            // ---- weights as A fragments: hi in row g4, lo in row g4 + 8 ----
+            // logical k 4*t4 + i <-> tokens (2t4, 2t4+1, 8+2t4, 9+2t4)[i]
+            // (+16 for registers 2 and 3), the token order of the S tiles
+            uint32_t pa[4];
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) {
+                uint32_t h0, q0, h1, q1;
+                split_e4m3x2(pr[2 * hk][0], pr[2 * hk][1], h0, q0);
+                split_e4m3x2(pr[2 * hk + 1][0], pr[2 * hk + 1][1], h1, q1);
+                pa[2 * hk] = h0 | (h1 << 16);
+                pa[2 * hk + 1] = q0 | (q1 << 16);
+            }
+            // ---- acc += P V ----
+            // A transposed ldmatrix of token rows gives lane (g4, t4) the
+            // byte pairs (dims 2g4, 2g4+1) of tokens 2t4 and 2t4+1 of each
+            // 8-token matrix; byte permutes regroup them into the even-dim
+            // and odd-dim B fragments in the weights' token order.  Masked
+            // token bytes are zeroed: the pool may hold NaN codes there.
+            const uint32_t vb = smem_u32(vbuf);
+            auto pv = [&](auto masked) {
+                uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+                if constexpr (decltype(masked)::value) {
+                    mk0 = token_bytemask(d.vmask >> (2 * t4));
+                    mk1 = token_bytemask(d.vmask >> (16 + 2 * t4));
+                }
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t r0, r1, r2, r3;     // tokens 0-7, 8-15, 16-23, 24-31 of column chunk c
+                    ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, c), r0, r1, r2, r3);
+                    uint32_t e0 = __byte_perm(r0, r1, 0x6420), o0 = __byte_perm(r0, r1, 0x7531);
+                    uint32_t e1 = __byte_perm(r2, r3, 0x6420), o1 = __byte_perm(r2, r3, 0x7531);
+                    if constexpr (decltype(masked)::value) {
+                        e0 &= mk0; o0 &= mk0; e1 &= mk1; o1 &= mk1;
+                    }
+                    mma_e4m3_16832(acc[2 * c], pa, e0, e1);
+                    mma_e4m3_16832(acc[2 * c + 1], pa, o0, o1);
+                }
+            };
+            if (d.vmask == 0xffffffffu) pv(std::false_type{});      // every token of the chunk is valid
+            else pv(std::true_type{});
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (d.flags & SEG_END) {
+                // hi + lo halves -> rows g4 (rows 8..15 are not stored)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    acc[nt][0] += acc[nt][2];
+                    acc[nt][1] += acc[nt][3];
+                }
+                finish_segment(p, d, acc, m0, -INFINITY, l0, 0.f, lane, rows_valid, out_h0);
+            }
         }
+    }
+
+    // The query tile as A fragments (m16n8k32 layout, head_dim in natural
+    // order): row g4 < G holds e4m3(2^e q) and row g4 + 8 the e4m3 residual;
+    // rows past the group are zero.  Returns 2^-e.
+    static __device__ __forceinline__ float load_q_e4m3(uint32_t (&qa)[KS8][4], const uint8_t* qbuf,
+                                                        int qrow_lo, int rows_valid, int lane, int q_tma,
+                                                        int qrows) {
+        const int g4 = lane >> 2, t4 = lane & 3;
+        auto qaddr = [&](int r, int c) -> uint32_t {
+            if (q_tma) {
+                const int rr = (c >> 3) * qrows + r;
+                return static_cast<uint32_t>(rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
+            }
+            return static_cast<uint32_t>(r * D * 2 + c * 16);
+        };
+        const int row = qrow_lo + min(g4, rows_valid - 1);
+        // dims 32ks + 16hk + 4t4 .. +3: 8 bytes of the query row
+        auto load4 = [&](int ks, int hk, float (&f)[4]) {
+            const int c = 4 * ks + 2 * hk + (t4 >> 1);
+            const uint2 u = *reinterpret_cast<const uint2*>(qbuf + qaddr(row, c) + 8 * (t4 & 1));
+            float2 f0, f1;
+            if constexpr (QT::code == PA_F16) {
+                f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+                f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            } else {
+                f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+                f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+            }
+            f[0] = f0.x; f[1] = f0.y; f[2] = f1.x; f[3] = f1.y;
+        };
+        // largest magnitude over the group's rows (lanes past it repeat a valid row)
+        float mx = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) {
+                float f[4];
+                load4(ks, hk, f);
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
+            }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int e = 0;
+        if (mx > 0.f && mx <= 3.0e38f) {
+            const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;   // floor(log2(mx))
+            e = max(-60, min(60, 7 - ex));
+        }
+        const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+        const bool pad = g4 >= rows_valid;
+#pragma unroll
+        for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) {
+                float f[4];
+                load4(ks, hk, f);
+                const float a0 = f[0] * sc, a1 = f[1] * sc, a2 = f[2] * sc, a3 = f[3] * sc;
+                const uint32_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
+                const uint32_t f01 = e4m3x2_to_f16x2(h01), f23 = e4m3x2_to_f16x2(h23);
+                const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
+                const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
+                const uint32_t l01 = f32x2_to_e4m3x2(a0 - b01.x, a1 - b01.y);
+                const uint32_t l23 = f32x2_to_e4m3x2(a2 - b23.x, a3 - b23.y);
+                qa[ks][2 * hk] = pad ? 0u : (h01 | (h23 << 16));
+                qa[ks][2 * hk + 1] = pad ? 0u : (l01 | (l23 << 16));
+            }
+        return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
     }
 
     // A fragments of this tile's query rows (16 x D) from the stage's query
@@ -792,7 +1054,7 @@ struct DecodeKernel {
             // ---- acc += p V over the chunk's valid tokens ----
             const int cidx = (lane * DPL * KV::bytes) / 16;           // 16-byte chunk holding my columns
             const int cbyte = (lane * DPL * KV::bytes) % 16;
-            for (int t = 0; t < CHUNK; ++t) {
+            for (int t = 0; t < CT; ++t) {
                 if (!((d.vmask >> t) & 1u)) continue;
                 const uint8_t* src = vbuf + lay.chunk_addr(lay.row_base(t, hl), t, cidx) + cbyte;
                 float vf[DPL];
@@ -879,11 +1141,11 @@ struct DecodeKernel {
     }
 };
 
-template <class KV, class QT, int D, bool TC>
+template <class KV, class QT, int D, bool TC, int CT>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
-    using K = DecodeKernel<KV, QT, D, TC>;
+    using K = DecodeKernel<KV, QT, D, TC, CT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + p.bar_off);
@@ -894,6 +1156,10 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     int4* s_first = reinterpret_cast<int4*>(scratch + 32);
     int2* s_tot = reinterpret_cast<int2*>(s_first + 1);
 
+    // The merge kernel is launched as a programmatic dependent of this one
+    // and waits (griddepcontrol.wait) for this grid to complete: letting it
+    // become resident now takes its launch off the critical path.
+    grid_dependents_launch();
     const int hg = blockIdx.x % p.NHG;
     const int range = blockIdx.x / p.NHG;
     Plan pl;
@@ -919,7 +1185,9 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         }
         K::producer(p, pl, hg, base, full, empty, qempty, descs, &tk, &tv, &tq);
     } else if (warp < p.NCW) {
-        if constexpr (TC) {
+        if constexpr (K::NATIVE8) {
+            K::consumer_e4m3(p, pl, hg, warp, base, full, empty, qempty, descs);
+        } else if constexpr (TC) {
             K::consumer_tc(p, pl, hg, warp, base, full, empty, qempty, descs);
         } else {
             K::consumer_simt(p, pl, hg, warp, base, full, empty, qempty, descs,
@@ -975,17 +1243,17 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
         const int h = (item % HG) * nw + warp;
         if (h >= p.Hq) continue;
         const int i = e.x, S = e.y, U = e.z, L = e.w;
-        const int n16 = cdiv_i(L, CHUNK), nu = n_units(L, p.P16);
+        const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
         OutT* o = static_cast<OutT*>(p.out) + (static_cast<size_t>(i) * p.Hq + h) * D + lane * DPL;
         float num[DPL];
 #pragma unroll
         for (int c = 0; c < DPL; ++c) num[c] = 0.f;
         float den = 0.f, M = -INFINITY;
-        if (p.P16 == 0 && C >= p.NR) {
+        if (p.PC == 0 && C >= p.NR) {
             // Common case: the partials are the consecutive slots of ranges
             // r0..r1.  Every lane loads all (m, l) pairs (broadcast) and its
             // columns of each partial at once, then merges locally.
-            const int r0 = range_of(S, C, p.NR), r1 = range_of(S + n16 - 1, C, p.NR);
+            const int r0 = range_of(S, C, p.NR), r1 = range_of(S + nch - 1, C, p.NR);
             const int base = r0 + U;
             const int n = min(r1 - r0 + 1, p.max_slots - base);
             for (int b0 = 0; b0 < n; b0 += NB) {
@@ -1065,8 +1333,8 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
         };
         int cnt = 0, my_slot = 0;
         for (int u = 0; u < nu; ++u) {
-            const int a = S + (p.P16 > 0 ? u * p.P16 : 0);
-            const int b = p.P16 > 0 ? min(a + p.P16, S + n16) : S + n16;
+            const int a = S + (p.PC > 0 ? u * p.PC : 0);
+            const int b = p.PC > 0 ? min(a + p.PC, S + nch) : S + nch;
             const int r0 = range_of(a, C, p.NR), r1 = range_of(b - 1, C, p.NR);
             for (int r = r0; r <= r1; ++r) {
                 const int slot = r + U + u;

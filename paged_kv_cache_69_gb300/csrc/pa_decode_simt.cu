@@ -9,16 +9,16 @@ namespace pa {
 
 const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D) {
 #define PA_SIMT_CASE(KVT, QTT)                                                                  \
-    if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 128, false>); \
-    if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 64, false>);   \
+    if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 128, false, 16>); \
+    if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 64, false, 16>);   \
     return nullptr;
     if (kv == PA_F32 && q == PA_F32) { PA_SIMT_CASE(F32T, F32T) }
     if (kv == PA_F16 && q == PA_F16) { PA_SIMT_CASE(F16T, F16T) }
     if (kv == PA_BF16 && q == PA_BF16) { PA_SIMT_CASE(BF16T, BF16T) }
     if (kv == PA_FP8_E4M3 && q == PA_F16 && D == 128)
-        return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, false>);
+        return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, false, 16>);
     if (kv == PA_FP8_E4M3 && q == PA_BF16 && D == 128)
-        return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, false>);
+        return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, false, 16>);
 #undef PA_SIMT_CASE
     return nullptr;
 }

@@ -9,16 +9,16 @@ namespace pa {
 
 const void* decode_kernel_tc(pa_dtype kv, pa_dtype q, int D) {
     if (kv == PA_F16 && q == PA_F16) {
-        if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<F16T, F16T, 128, true>);
-        if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<F16T, F16T, 64, true>);
+        if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<F16T, F16T, 128, true, 16>);
+        if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<F16T, F16T, 64, true, 16>);
     }
     if (kv == PA_BF16 && q == PA_BF16) {
-        if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<BF16T, BF16T, 128, true>);
-        if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<BF16T, BF16T, 64, true>);
+        if (D == 128) return reinterpret_cast<const void*>(&pa_decode_kernel<BF16T, BF16T, 128, true, 16>);
+        if (D == 64) return reinterpret_cast<const void*>(&pa_decode_kernel<BF16T, BF16T, 64, true, 16>);
     }
     if (kv == PA_FP8_E4M3 && D == 128) {
-        if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, true>);
-        if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, true>);
+        if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, true, 16>);
+        if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, true, 16>);
     }
     return nullptr;
 }

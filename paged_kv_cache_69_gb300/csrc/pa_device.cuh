@@ -184,6 +184,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// D += A B with fp8-e4m3 operands and an fp32 accumulator, m16n8k32
+// (PTX ISA: mma, .e4m3 element type).  A holds 16 rows x 32 k as four
+// registers of four bytes (row g, k 4t..4t+3 | row g+8, same k | row g,
+// k 16+4t.. | row g+8, k 16+4t..); B holds 32 k x 8 columns as two registers
+// (column g, k 4t..4t+3 | k 16+4t..), with g = lane / 4, t = lane % 4.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats to two e4m3 bytes (lo -> low byte), round to nearest even,
+// saturating to +-448 (PTX ISA: cvt, .e4m3x2 destination).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// f16x2 (low half -> low byte) to two e4m3 bytes, same rounding.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+    return r;
+}
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // 128-byte TMA swizzle: within each 1024-byte atom, the 16-byte chunk index
 // of a 128-byte row is XOR-ed with the row index modulo 8.

@@ -7,5 +7,7 @@ namespace pa {
 // Kernel entry for the given cache dtype, query dtype and head_dim, or null.
 const void* decode_kernel_tc(pa_dtype kv, pa_dtype q, int D);
 const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D);
+// fp8-e4m3 cache, tensor cores with e4m3 operands, 32-token chunks.
+const void* decode_kernel_e4m3(pa_dtype q, int D);
 const void* reduce_kernel(pa_dtype out, int D);
 }  // namespace pa

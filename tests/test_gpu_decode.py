@@ -49,6 +49,9 @@ CASES = [
     ("f16", None, 128, 32, 64, 4, [70, 1030]),             # G = 16
     ("fp8_e4m3", "bf16", 128, 32, 32, 8, [1, 31, 32, 33, 900]),
     ("fp8_e4m3", "f16", 128, 16, 28, 4, [5, 16, 17, 400]),
+    ("fp8_e4m3", "bf16", 128, 8, 16, 4, [1, 8, 9, 31, 32, 33, 300]),   # four 8-row boxes per 32-token chunk
+    ("fp8_e4m3", "bf16", 128, 16, 8, 8, [2, 47, 64, 65]),             # G = 1
+    ("fp8_e4m3", "f16", 128, 16, 32, 2, [7, 100, 513]),               # G = 16: e4m3 -> f16 kernel
     ("f32", None, 128, 16, 8, 2, [3, 17, 90]),
     ("f32", None, 64, 8, 6, 3, [1, 8, 9, 64]),
 ]
@@ -69,6 +72,23 @@ def test_decode_small(case, variant, partition_tokens):
         pytest.skip("f32 caches run on the CUDA-core path")
     wl = _case(*case, seed=len(case[6]))
     _full_check(wl, simt=(variant == "simt"), partition_tokens=partition_tokens)
+
+
+@pytest.mark.parametrize("partition_tokens", [48, 64, 96])
+def test_fp8_partitions(partition_tokens):
+    """fp8 caches: partitions that are multiples of 32 run the native-e4m3
+    kernel (32-token chunks), odd multiples of 16 the e4m3 -> f16 kernel."""
+    wl = _case("fp8_e4m3", "bf16", 128, 16, 32, 8, [1, 47, 48, 49, 95, 96, 97, 1000], seed=12)
+    _full_check(wl, partition_tokens=partition_tokens)
+
+
+def test_fp8_query_scale_extremes():
+    """The native-e4m3 kernel scales each query tile by a power of two: tiny
+    and large query magnitudes give the same relative accuracy."""
+    for qd, mag, seed in (("f16", 1e-4, 13), ("bf16", 1e-4, 14), ("bf16", 100.0, 15)):
+        wl = _case("fp8_e4m3", qd, 128, 16, 28, 4, [33, 250], seed=seed)
+        wl.q = (wl.q.float() * mag).to(wl.q.dtype)
+        _full_check(wl)
 
 
 def test_one_long_sequence_spans_every_cta():
@@ -248,5 +268,6 @@ def test_full_long_context(kv):
 
 
 @pytest.mark.slow
-def test_full_long_context_512_token_partitions():
-    _sampled_check(inputs.long_ctx("bf16", gen_device="cuda", needles=4), samples=8, partition_tokens=512)
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_full_long_context_512_token_partitions(kv):
+    _sampled_check(inputs.long_ctx(kv, gen_device="cuda", needles=4), samples=8, partition_tokens=512)
