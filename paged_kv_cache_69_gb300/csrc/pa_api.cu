@@ -182,7 +182,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
                        : tc    ? decode_kernel_tc(kv_dtype, q_dtype, D)
                                : decode_kernel_simt(kv_dtype, q_dtype, D);
     if (!kern) return fail(PA_ERR_UNSUPPORTED, "decode: no kernel for this dtype / head_dim combination");
-    const void* rkern = reduce_kernel(q_dtype, D);
+    const bool split_heads = partition_tokens > 0;
+    const void* rkern = reduce_kernel(q_dtype, D, split_heads);
     if (!rkern) return fail(PA_ERR_UNSUPPORTED, "decode: no reduce kernel for this output dtype");
     DeviceInfo dev;
     if (!device_info(dev)) return fail(PA_ERR_CUDA, "decode: cannot query the current device");
@@ -214,6 +215,11 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.HPC = HPC; p.NHG = NHG; p.MT = MT; p.NCW = NCW;
     p.ct = CT;
     p.PC = partition_tokens / CT;
+    // Schedule weights: a unit start (query rows loaded, result written)
+    // is charged 3/4 of a chunk, which balanced CTA finish times best on
+    // length mixes with many short sequences.
+    p.WQ = 4;
+    p.WS = 3;
     p.rpb = rpb;
     p.box_bytes = static_cast<uint32_t>(rpb * HPC * DH * 128);
     p.kv_bytes = static_cast<uint32_t>(CT * HPC * D * e);
@@ -336,7 +342,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         int red_per_sm = 0;
         ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&red_per_sm, rkern, RED_THREADS, 0);
         if (ce != cudaSuccess) return fail_cuda("decode: reduce occupancy query", ce);
-        const long long items = static_cast<long long>(B) * ((Hq + RED_THREADS / 32 - 1) / (RED_THREADS / 32));
+        const long long items = split_heads ? static_cast<long long>(B) * Hq
+                                            : static_cast<long long>(B) * ((Hq + RED_THREADS / 32 - 1) / (RED_THREADS / 32));
         const long long g = std::max(1LL, std::min(items, static_cast<long long>(std::max(1, red_per_sm)) * dev.sms));
         rcfg.gridDim = dim3(static_cast<unsigned>(g));
     }

@@ -40,7 +40,11 @@ constexpr int MAX_STAGES = 8;
 constexpr int NQ = 2;                // query-row ring slots
 constexpr int MAX_WARPS = 9;         // up to 8 consumers + 1 producer
 
-enum : uint32_t { SEG_START = 1u, SEG_END = 2u, DIRECT = 4u };
+// GAP: this segment ends the CTA's range exactly at a partition end while
+// its sequence continues in the next range; the slot after the segment's
+// would stay unwritten, so the segment also writes an empty partial there
+// (m = -inf, l = 0, acc = 0), keeping every sequence's partials consecutive.
+enum : uint32_t { SEG_START = 1u, SEG_END = 2u, DIRECT = 4u, GAP = 8u };
 
 struct StageDesc {
     int seq;
@@ -59,7 +63,8 @@ struct DecodeParams {
     const int32_t* seq_lens;
     float* part_acc;          // [max_slots][Hq][D]
     float2* part_ml;          // [max_slots][Hq]  (m in log2 units, l)
-    int4* split_list;         // [B] (seq, first chunk, first unit, length) of sequences needing a merge
+    int4* split_list;         // [B] sequences needing a merge: (seq, first slot, slot count, -1) when
+                              // their partials are consecutive slots, else (seq, first chunk, first unit, length)
     int* totals;              // [0] chunks, [1] units, [2] entries in split_list
     int32_t* err_flag;
     int B, Hq, Hkv, G, D, bs, NB, MB;
@@ -67,6 +72,7 @@ struct DecodeParams {
     int HPC, NHG, NR, MT, NCW;
     int ct;                   // tokens per chunk (pipeline stage): 16, or 32 for native e4m3
     int PC;                   // partition length in chunks, 0 = none
+    int WQ, WS;               // schedule weights of a chunk and of a unit start
     int max_slots;
     float qk_scale;           // scale * log2(e) (* k_scale for fp8)
     float v_scale;            // v_scale for fp8, else 1
@@ -93,19 +99,51 @@ __device__ __forceinline__ int n_units(int L, int PC, int ct) {
     const int nch = cdiv_i(L, ct);
     return nch == 0 ? 0 : (PC > 0 ? cdiv_i(nch, PC) : 1);
 }
-// The range (CTA column) owning global chunk c: largest r with
-// floor(r * C / NR) <= c.
-__device__ __forceinline__ int range_of(int c, int C, int NR) {
-    if (static_cast<long long>(C) * NR < 0x7fffffffLL)       // 32-bit division when it cannot overflow
-        return static_cast<int>((static_cast<unsigned>(c + 1) * static_cast<unsigned>(NR) - 1u) /
-                                static_cast<unsigned>(C));
-    return static_cast<int>(((static_cast<long long>(c) + 1) * NR - 1) / C);
+// Cost-weighted chunk stream.  Chunk k (global index) of global unit gu sits
+// at position WQ*k + WS*(gu + 1): each chunk weighs WQ and each unit start WS
+// more, for the per-segment work (query rows in, result out).  With
+// W = WQ*C + WS*Ut over all C chunks and Ut units, range r (one CTA column)
+// takes the chunks whose positions lie in [floor(r*W/NR), floor((r+1)*W/NR)):
+// contiguous chunk intervals of about equal cost.
+__device__ __forceinline__ long long stream_weight(const DecodeParams& p, int C, int Ut) {
+    return static_cast<long long>(p.WQ) * C + static_cast<long long>(p.WS) * Ut;
 }
-// Range r covers chunks [floor(r*C/NR), floor((r+1)*C/NR)); with more
-// ranges than chunks some are empty and write no partial.
-__device__ __forceinline__ bool range_empty(int r, int C, int NR) {
-    if (C >= NR) return false;                                // every range holds a chunk
-    return static_cast<long long>(r) * C / NR == (static_cast<long long>(r) + 1) * C / NR;
+__device__ __forceinline__ long long chunk_pos(const DecodeParams& p, int k, int gu) {
+    return static_cast<long long>(p.WQ) * k + static_cast<long long>(p.WS) * (gu + 1);
+}
+// (Divisions run in 32 bits whenever W * NR fits, as it does for any
+// realistic batch; 64-bit integer division is several times slower.)
+__device__ __forceinline__ bool fits32(long long W, int NR) {
+    return W * NR < 0x7fffffffLL;
+}
+__device__ __forceinline__ long long range_lo(int r, long long W, int NR) {
+    if (fits32(W, NR))
+        return static_cast<unsigned>(r) * static_cast<unsigned>(W) / static_cast<unsigned>(NR);
+    return static_cast<long long>(r) * W / NR;
+}
+// the range holding weighted position pos: largest r with range_lo(r) <= pos
+__device__ __forceinline__ int range_of_pos(long long pos, long long W, int NR) {
+    if (fits32(W, NR))
+        return static_cast<int>((static_cast<unsigned>(pos + 1) * static_cast<unsigned>(NR) - 1u) /
+                                static_cast<unsigned>(W));
+    return static_cast<int>(((pos + 1) * NR - 1) / W);
+}
+// first chunk k in [a, b) of a unit (positions WQ*k + base) with position >= t
+__device__ __forceinline__ int first_chunk_from(long long t, int a, long long base, int WQ) {
+    const long long d = t - base;
+    long long k = 0;
+    if (d > 0) k = d < 0x7fffffffLL ? static_cast<long long>((static_cast<unsigned>(d) + WQ - 1) / WQ) : (d + WQ - 1) / WQ;
+    return static_cast<int>(k > a ? k : a);
+}
+// Every range spans at least WQ + WS positions, the largest gap between
+// consecutive chunks, so no range is empty.
+__device__ __forceinline__ bool dense_ranges(const DecodeParams& p, long long W) {
+    return W >= static_cast<long long>(p.WQ + p.WS) * p.NR;
+}
+// does range r hold a chunk of the unit [a, b) with base offset `base`?
+__device__ __forceinline__ bool unit_in_range(int r, int a, int b, long long base, long long W, int NR, int WQ) {
+    const int k = first_chunk_from(range_lo(r, W, NR), a, base, WQ);
+    return k < b && static_cast<long long>(WQ) * k + base < range_lo(r + 1, W, NR);
 }
 
 // ---------------------------------------------------------------------------
@@ -130,7 +168,7 @@ __device__ __forceinline__ void warp_scan_pair(int& a, int& b) {
 }
 
 __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch, int4* s_first, int2* s_tot,
-                          Plan& plan) {
+                                 int* s_end, Plan& plan) {
     const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = nth >> 5;
     const int maxL = p.MB * p.bs;
@@ -150,7 +188,7 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
     int ci = csum, ui = usum;           // inclusive within the warp
     warp_scan_pair(ci, ui);
     if (lane == 31) scratch[warp] = make_int2(ci, ui);
-    if (tid == 0) *s_first = make_int4(-1, 0, 0, 0);
+    if (tid == 0) { *s_first = make_int4(-1, 0, 0, 0); *s_end = INT_MAX; }
     __syncthreads();
     if (warp == 0) {
         int2 v = lane < nwarps ? scratch[lane] : make_int2(0, 0);
@@ -163,16 +201,53 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
     const int2 wpre = scratch[warp];
     const int cpre = wpre.x + ci - csum, upre = wpre.y + ui - usum;       // exclusive per thread
     const int C = s_tot->x, Ut = s_tot->y;
-    const int cs = static_cast<int>(static_cast<long long>(range) * C / p.NR);
-    const int ce = static_cast<int>(static_cast<long long>(range + 1) * C / p.NR);
-    if (cs < ce && cpre <= cs && cs < cpre + csum) {
-        int S = cpre, U = upre;
-        for (int i = i0; i < i1; ++i) {
-            const int L = clamp_len(p.seq_lens[i], maxL);
-            const int nch = cdiv_i(L, p.ct);
-            if (cs < S + nch) { *s_first = make_int4(i, S, U, 0); break; }
-            S += nch;
-            U += n_units(L, p.PC, p.ct);
+    const long long W = stream_weight(p, C, Ut);
+    // The range starts at the first chunk with position >= lo and ends at
+    // the first with position >= hi; the thread whose sequences hold such a
+    // chunk records it.
+    const long long lo = range_lo(range, W, p.NR), hi = range_lo(range + 1, W, p.NR);
+    if (csum > 0) {
+        const long long prev_last = cpre > 0 ? chunk_pos(p, cpre - 1, upre - 1) : -1;
+        const long long my_last = chunk_pos(p, cpre + csum - 1, upre + usum - 1);
+        const bool has_lo = prev_last < lo && lo <= my_last;
+        const bool has_hi = prev_last < hi && hi <= my_last;
+        if (has_lo || has_hi) {
+            int S = cpre, U = upre;
+            bool need_lo = has_lo, need_hi = has_hi;
+            // the first chunk of sequence (S, U, nch, nu) at or after
+            // position t, or -1 if its last chunk lies before t
+            auto find = [&](long long t, int S, int U, int nch, int nu) -> int {
+                int u = 0;
+                if (p.PC > 0 && nu > 1) {
+                    // last chunk of unit u < nu-1 sits at
+                    // (WQ*PC + WS)*(u+1) + WQ*(S-1) + WS*U
+                    const long long step = static_cast<long long>(p.WQ) * p.PC + p.WS;
+                    const long long d = t - (static_cast<long long>(p.WQ) * (S - 1) + static_cast<long long>(p.WS) * U);
+                    const long long uu = d <= step ? 0 : (d + step - 1) / step - 1;
+                    u = static_cast<int>(uu < nu - 1 ? uu : nu - 1);
+                }
+                const int a = S + (p.PC > 0 ? u * p.PC : 0);
+                const int b = p.PC > 0 ? min(a + p.PC, S + nch) : S + nch;
+                const long long base = static_cast<long long>(p.WS) * (U + u + 1);
+                if (t > static_cast<long long>(p.WQ) * (b - 1) + base) return -1;
+                return first_chunk_from(t, a, base, p.WQ);
+            };
+            for (int i = i0; i < i1 && (need_lo || need_hi); ++i) {
+                const int L = clamp_len(p.seq_lens[i], maxL);
+                const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
+                if (nch > 0) {
+                    if (need_lo) {
+                        const int k = find(lo, S, U, nch, nu);
+                        if (k >= 0) { *s_first = make_int4(i, S, U, k); need_lo = false; }
+                    }
+                    if (need_hi) {
+                        const int k = find(hi, S, U, nch, nu);
+                        if (k >= 0) { *s_end = k; need_hi = false; }
+                    }
+                }
+                S += nch;
+                U += nu;
+            }
         }
     }
     if (blockIdx.x == 0) {
@@ -186,8 +261,21 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
                 uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
                                                     static_cast<size_t>(i) * p.Hq * p.D * p.out_bytes);
                 for (int k = 0; k < p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
-            } else if (!(nu == 1 && range_of(S, C, p.NR) == range_of(S + nch - 1, C, p.NR))) {
-                p.split_list[atomicAdd(&p.totals[2], 1)] = make_int4(i, S, U, L);
+            } else {
+                const int r0 = range_of_pos(chunk_pos(p, S, U), W, p.NR);
+                const int r1 = range_of_pos(chunk_pos(p, S + nch - 1, U + nu - 1), W, p.NR);
+                if (nu > 1 || r0 != r1) {
+                    // The partials sit in consecutive slots r0 + U ..
+                    // r1 + U + nu - 1 when every range between r0 and r1
+                    // holds a chunk of the sequence (GAP segments fill the
+                    // slots skipped at range ends that meet partition ends).
+                    int4 e = make_int4(i, S, U, L);
+                    if ((nu == 1 && C >= p.NR) || dense_ranges(p, W)) {
+                        const int first = r0 + U, last = r1 + U + nu - 1;
+                        e = make_int4(i, first, min(last - first + 1, p.max_slots - first), -1);
+                    }
+                    p.split_list[atomicAdd(&p.totals[2], 1)] = e;
+                }
             }
             S += nch;
             U += nu;
@@ -196,7 +284,9 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
     }
     __syncthreads();
     const int4 f = *s_first;
-    plan.cs = cs; plan.ce = ce; plan.seq = f.x; plan.S = f.y; plan.U = f.z;
+    plan.cs = f.x >= 0 ? f.w : C;
+    plan.ce = min(*s_end, C);
+    plan.seq = f.x; plan.S = f.y; plan.U = f.z;
     plan.C = C; plan.Ut = Ut;
 }
 
@@ -360,6 +450,7 @@ struct DecodeKernel {
                                          (p.PC > 0 && (j + 1) % p.PC == 0);
                     if (seg_start) flags |= SEG_START;
                     if (seg_end) flags |= SEG_END;
+                    if (k == pl.ce - 1 && p.PC > 0 && (j + 1) % p.PC == 0 && j + 1 < nch) flags |= GAP;
                     const int nu = n_units(L, p.PC, p.ct);
                     if (nu == 1 && Si >= pl.cs && Si + nch <= pl.ce) flags |= DIRECT;
                     StageDesc d;
@@ -502,7 +593,18 @@ struct DecodeKernel {
                 if (g4 < rows_valid) ml[out_h0 + g4] = make_float2(m0, lt0);
                 if (g4 + 8 < rows_valid) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
             }
+            if (!direct && (d.flags & GAP)) write_empty_partial(p, d.slot + 1, out_h0, rows_valid, lane);
         }
+    }
+
+    // An empty partial (m = -inf, l = 0, acc = 0) for `rows` query heads
+    // from out_h0 at `slot`.
+    static __device__ __forceinline__ void write_empty_partial(const DecodeParams& p, int slot, int out_h0,
+                                                               int rows, int lane) {
+        if (slot >= p.max_slots) return;
+        float4* acc = reinterpret_cast<float4*>(p.part_acc + (static_cast<size_t>(slot) * p.Hq + out_h0) * D);
+        for (int e = lane; e < rows * D / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < rows) p.part_ml[static_cast<size_t>(slot) * p.Hq + out_h0 + lane] = make_float2(-INFINITY, 0.f);
     }
 
     // ---------------- tensor-core consumer ----------------
@@ -1093,6 +1195,7 @@ struct DecodeKernel {
                             if (lane == 0) ml[out_h0 + r] = make_float2(m[r], l[r]);
                         }
                     }
+                    if (d.flags & GAP) write_empty_partial(p, d.slot + 1, out_h0, nr, lane);
                 }
             }
             __syncwarp();
@@ -1155,6 +1258,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     int2* scratch = reinterpret_cast<int2*>(descs + MAX_STAGES);
     int4* s_first = reinterpret_cast<int4*>(scratch + 32);
     int2* s_tot = reinterpret_cast<int2*>(s_first + 1);
+    int* s_end = reinterpret_cast<int*>(s_tot + 1);
 
     // The merge kernel is launched as a programmatic dependent of this one
     // and waits (griddepcontrol.wait) for this grid to complete: letting it
@@ -1163,7 +1267,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     const int hg = blockIdx.x % p.NHG;
     const int range = blockIdx.x / p.NHG;
     Plan pl;
-    make_plan(p, range, scratch, s_first, s_tot, pl);
+    make_plan(p, range, scratch, s_first, s_tot, s_end, pl);
     if (pl.cs >= pl.ce || pl.seq < 0) return;
 
     const int warp = threadIdx.x >> 5;
@@ -1225,80 +1329,39 @@ __device__ __forceinline__ float2 ldg_f2(const float2* p) {
 
 constexpr int RED_THREADS = 128;     // 4 warps: one query head each
 
-template <typename OutT, int D>
+// WPI warps per (sequence, head): 1 when sequences have a handful of
+// partials (each warp of the CTA takes one head), RED_THREADS / 32 when
+// partitioned sequences have hundreds (the CTA's warps split one head's
+// partials and combine their results through shared memory).
+template <typename OutT, int D, int WPI>
 __global__ void __launch_bounds__(RED_THREADS)
 pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int DPL = D / 32;
-    constexpr int NB = 16;               // partials whose rows load together
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int HG = cdiv_i(p.Hq, nw);     // head groups of nw heads
+    constexpr int NB = 16;               // partials merged per batch, one per lane
+    constexpr int NW = RED_THREADS / 32;
+    constexpr int HPB = NW / WPI;        // heads per CTA
+    static_assert(WPI == 1 || HPB == 1, "split heads take the whole CTA");
+    __shared__ float comb[WPI > 1 ? NW * 32 * (DPL + 2) : 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = warp % WPI;
+    const int HG = cdiv_i(p.Hq, HPB);    // head groups of HPB heads
     grid_dependency_wait();
     for (int item = blockIdx.x;; item += gridDim.x) {
         // the count and this item's list entry load together
-        // the count, the chunk total and this item's list entry load together
         const int count = *reinterpret_cast<volatile int*>(&p.totals[2]);
-        const int C = p.totals[0];
         const int4 e = p.split_list[min(item / HG, p.B - 1)];
         if (item >= count * HG) break;
-        const int h = (item % HG) * nw + warp;
-        if (h >= p.Hq) continue;
-        const int i = e.x, S = e.y, U = e.z, L = e.w;
-        const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
-        OutT* o = static_cast<OutT*>(p.out) + (static_cast<size_t>(i) * p.Hq + h) * D + lane * DPL;
+        const int h = (item % HG) * HPB + warp / WPI;
+        if (WPI == 1 && h >= p.Hq) continue;
+        OutT* o = static_cast<OutT*>(p.out) + (static_cast<size_t>(e.x) * p.Hq + h) * D + lane * DPL;
         float num[DPL];
 #pragma unroll
         for (int c = 0; c < DPL; ++c) num[c] = 0.f;
         float den = 0.f, M = -INFINITY;
-        if (p.PC == 0 && C >= p.NR) {
-            // Common case: the partials are the consecutive slots of ranges
-            // r0..r1.  Every lane loads all (m, l) pairs (broadcast) and its
-            // columns of each partial at once, then merges locally.
-            const int r0 = range_of(S, C, p.NR), r1 = range_of(S + nch - 1, C, p.NR);
-            const int base = r0 + U;
-            const int n = min(r1 - r0 + 1, p.max_slots - base);
-            for (int b0 = 0; b0 < n; b0 += NB) {
-                float2 ml[NB];
-                float v[NB][DPL];
-#pragma unroll
-                for (int t = 0; t < NB; ++t)
-                    ml[t] = (b0 + t < n) ? ldg_f2(p.part_ml + static_cast<size_t>(base + b0 + t) * p.Hq + h)
-                                         : make_float2(-INFINITY, 0.f);
-#pragma unroll
-                for (int t = 0; t < NB; ++t) {
-                    if (b0 + t < n) {
-                        VecF<DPL>::load(p.part_acc + (static_cast<size_t>(base + b0 + t) * p.Hq + h) * D + lane * DPL, v[t]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < DPL; ++c) v[t][c] = 0.f;
-                    }
-                }
-                float Mn = M;
-#pragma unroll
-                for (int t = 0; t < NB; ++t) Mn = fmaxf(Mn, ml[t].x);
-                const float Mu = (Mn == -INFINITY) ? 0.f : Mn;
-                const float sold = exp2f(M - Mu);
-                den *= sold;
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) num[c] *= sold;
-#pragma unroll
-                for (int t = 0; t < NB; ++t) {
-                    const float wt = exp2f(ml[t].x - Mu);      // 0 for padding (m = -inf)
-                    den = fmaf(wt, ml[t].y, den);
-#pragma unroll
-                    for (int c = 0; c < DPL; ++c) num[c] = fmaf(wt, v[t][c], num[c]);
-                }
-                M = Mn;
-            }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-            for (int c = 0; c < DPL; ++c) o[c] = from_float<OutT>(num[c] * inv);
-            continue;
-        }
-        // Up to NB partials per batch, one per lane: their (m, l) and their
-        // accumulator rows are independent loads issued together.
+        // Merge n <= NB partials; lane t names the slot of partial t.  The
+        // (m, l) pair of each partial (one per lane) and every lane's
+        // columns of all n partials are independent loads issued together.
         auto merge = [&](int n, int my_slot) {
-            float2 ml = make_float2(-INFINITY, 0.f);
-            if (lane < n) ml = p.part_ml[static_cast<size_t>(my_slot) * p.Hq + h];
             float v[NB][DPL];
 #pragma unroll
             for (int t = 0; t < NB; ++t) {
@@ -1310,6 +1373,8 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
                     for (int c = 0; c < DPL; ++c) v[t][c] = 0.f;
                 }
             }
+            const float2 ml = lane < n ? ldg_f2(p.part_ml + static_cast<size_t>(my_slot) * p.Hq + h)
+                                       : make_float2(-INFINITY, 0.f);
             float bm = ml.x;
 #pragma unroll
             for (int o2 = 16; o2 > 0; o2 >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o2));
@@ -1331,19 +1396,58 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
             }
             M = Mn;
         };
-        int cnt = 0, my_slot = 0;
-        for (int u = 0; u < nu; ++u) {
-            const int a = S + (p.PC > 0 ? u * p.PC : 0);
-            const int b = p.PC > 0 ? min(a + p.PC, S + nch) : S + nch;
-            const int r0 = range_of(a, C, p.NR), r1 = range_of(b - 1, C, p.NR);
-            for (int r = r0; r <= r1; ++r) {
-                const int slot = r + U + u;
-                if (range_empty(r, C, p.NR) || slot >= p.max_slots) continue;
-                if ((cnt % NB) == lane) my_slot = slot;
-                if ((++cnt % NB) == 0) merge(NB, my_slot);
+        if (e.w < 0) {
+            // consecutive slots e.y .. e.y + e.z - 1, a contiguous share per warp
+            const int per = cdiv_i(e.z, WPI), lo = min(e.z, sub * per), hi = min(e.z, lo + per);
+            for (int b0 = lo; b0 < hi; b0 += NB) merge(min(NB, hi - b0), e.y + b0 + lane);
+        } else if (sub == 0) {
+            // Partials of sequence i lie at slot range + first_unit + unit for
+            // every range holding chunks of the unit.
+            const int S = e.y, U = e.z, L = e.w;
+            const int C = p.totals[0], Ut = p.totals[1];
+            const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
+            const long long W = stream_weight(p, C, Ut);
+            int cnt = 0, my_slot = 0;
+            for (int u = 0; u < nu; ++u) {
+                const int a = S + (p.PC > 0 ? u * p.PC : 0);
+                const int b = p.PC > 0 ? min(a + p.PC, S + nch) : S + nch;
+                const long long base = static_cast<long long>(p.WS) * (U + u + 1);
+                const int r0 = range_of_pos(static_cast<long long>(p.WQ) * a + base, W, p.NR);
+                const int r1 = range_of_pos(static_cast<long long>(p.WQ) * (b - 1) + base, W, p.NR);
+                for (int r = r0; r <= r1; ++r) {
+                    const int slot = r + U + u;
+                    // ranges may be empty unless they are dense: skip those
+                    // without a chunk of the unit
+                    if (slot >= p.max_slots || (!dense_ranges(p, W) && !unit_in_range(r, a, b, base, W, p.NR, p.WQ)))
+                        continue;
+                    if ((cnt % NB) == lane) my_slot = slot;
+                    if ((++cnt % NB) == 0) merge(NB, my_slot);
+                }
             }
+            if (cnt % NB) merge(cnt % NB, my_slot);
         }
-        if (cnt % NB) merge(cnt % NB, my_slot);
+        if constexpr (WPI > 1) {
+            float* mine = comb + (warp * 32 + lane) * (DPL + 2);
+            mine[0] = M; mine[1] = den;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) mine[2 + c] = num[c];
+            __syncthreads();
+            if (sub == 0) {
+                for (int w2 = 1; w2 < WPI; ++w2) {
+                    const float* o2 = comb + ((warp + w2) * 32 + lane) * (DPL + 2);
+                    const float M2 = o2[0];
+                    const float Mn = fmaxf(M, M2);
+                    const float Mu = (Mn == -INFINITY) ? 0.f : Mn;
+                    const float s1 = exp2f(M - Mu), s2 = exp2f(M2 - Mu);
+                    den = den * s1 + o2[1] * s2;
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) num[c] = num[c] * s1 + o2[2 + c] * s2;
+                    M = Mn;
+                }
+            }
+            __syncthreads();                  // the buffer is reused by the next item
+            if (sub != 0) continue;
+        }
         const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
         for (int c = 0; c < DPL; ++c) o[c] = from_float<OutT>(num[c] * inv);

@@ -23,13 +23,17 @@ const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D) {
     return nullptr;
 }
 
-const void* reduce_kernel(pa_dtype out, int D) {
-    if (out == PA_F32) return D == 128 ? reinterpret_cast<const void*>(&pa_reduce_kernel<float, 128>)
-                                       : reinterpret_cast<const void*>(&pa_reduce_kernel<float, 64>);
-    if (out == PA_F16) return D == 128 ? reinterpret_cast<const void*>(&pa_reduce_kernel<__half, 128>)
-                                       : reinterpret_cast<const void*>(&pa_reduce_kernel<__half, 64>);
-    if (out == PA_BF16) return D == 128 ? reinterpret_cast<const void*>(&pa_reduce_kernel<__nv_bfloat16, 128>)
-                                        : reinterpret_cast<const void*>(&pa_reduce_kernel<__nv_bfloat16, 64>);
+const void* reduce_kernel(pa_dtype out, int D, bool split_heads) {
+#define PA_RED(T) \
+    if (D == 128) return split_heads ? reinterpret_cast<const void*>(&pa_reduce_kernel<T, 128, RED_THREADS / 32>) \
+                                     : reinterpret_cast<const void*>(&pa_reduce_kernel<T, 128, 1>);          \
+    if (D == 64) return split_heads ? reinterpret_cast<const void*>(&pa_reduce_kernel<T, 64, RED_THREADS / 32>)  \
+                                    : reinterpret_cast<const void*>(&pa_reduce_kernel<T, 64, 1>);            \
+    return nullptr;
+    if (out == PA_F32) { PA_RED(float) }
+    if (out == PA_F16) { PA_RED(__half) }
+    if (out == PA_BF16) { PA_RED(__nv_bfloat16) }
+#undef PA_RED
     return nullptr;
 }
 

@@ -91,6 +91,24 @@ def test_fp8_query_scale_extremes():
         _full_check(wl)
 
 
+@pytest.mark.parametrize("variant", ["tc", "simt"])
+@pytest.mark.parametrize("kv,Hq,Hkv,lens,pt", [
+    # dense ranges (every range holds a chunk): range ends that meet
+    # partition ends leave a slot that the segment fills with an empty partial
+    ("bf16", 32, 8, [2900, 3100, 1700, 4096, 2222, 3333, 1000, 2500], 32),
+    ("f16", 28, 4, [4000, 3999, 4001, 2500, 5000, 1234, 3000, 4444], 32),
+    ("fp8_e4m3", 32, 8, [2900, 3100, 1700, 4096, 2222, 3333, 1000, 2500], 64),
+    # sparse ranges: about one chunk per range, so ranges can fall between
+    # two partitions and hold nothing
+    ("bf16", 32, 8, [680, 690, 700, 675], 32),
+    ("f16", 28, 4, [1400, 1410, 1390, 1420], 32),
+])
+def test_partition_slot_layouts(variant, kv, Hq, Hkv, lens, pt):
+    qd = "bf16" if kv == "fp8_e4m3" else None
+    wl = _case(kv, qd, 128, 16, Hq, Hkv, lens, seed=sum(lens) % 1000)
+    _full_check(wl, simt=(variant == "simt"), partition_tokens=pt)
+
+
 def test_one_long_sequence_spans_every_cta():
     wl = _case("bf16", None, 128, 16, 8, 1, [40000], seed=3)
     _full_check(wl)
