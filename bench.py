@@ -77,11 +77,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources the decode kernels (main + merge) and their launch code are built from
+DECODE_SOURCES = ("pa_api.cu", "pa_common.h", "pa_decode_e4m3.cu", "pa_decode_kernel.cuh", "pa_decode_simt.cu",
+                  "pa_decode_tc.cu", "pa_device.cuh", "pa_kernels.h")
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_69_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_69_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
