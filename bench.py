@@ -382,6 +382,68 @@ def run_ours(args, rank, world, local) -> dict | None:
     return res
 
 
+# ---------------------------------------------------------------------------
+# host block manager (the allocator that feeds the GPU calls)
+# ---------------------------------------------------------------------------
+def _bm_trace(n_req: int, bs: int, seed: int):
+    """Prompt token lists of a short-mix batch whose prompts start with one of
+    four shared 256-token system prompts (prefix-cache hits)."""
+    import random
+    from paged_kv_cache_69_gb300 import inputs
+    rnd = random.Random(seed)
+    systems = [[rnd.randrange(150000) for _ in range(256)] for _ in range(4)]
+    lens = inputs.short_mix_lens(seed, n_req)
+    return [systems[i % 4] + [rnd.randrange(150000) for _ in range(L)] for i, L in enumerate(lens)]
+
+
+def _bm_run(make, hash_fn, prompts, bs, decode_steps, reqs_cap=None):
+    """Admit every prompt (prefix lookup + allocation), then decode_steps
+    steps of one token per request with the step's block tables; returns
+    (admit seconds, seconds per decode step, requests admitted)."""
+    import numpy as np
+    from paged_kv_cache_69_gb300 import block_manager as hbm
+    m = make()
+    prompts = prompts[:reqs_cap] if reqs_cap else prompts
+    t0 = time.perf_counter()
+    for r, p in enumerate(prompts):
+        m.allocate(r, len(p), hash_fn(p, bs))
+    t1 = time.perf_counter()
+    reqs = np.arange(len(prompts), dtype=np.int64)
+    maxb = max(-(-(len(p) + decode_steps) // bs) for p in prompts)
+    tables = hbm.BlockTableBuffer(len(prompts), maxb) if hasattr(m, "append_slots") else None
+    for _ in range(decode_steps):
+        if tables is not None:
+            m.append_slots(reqs)
+            tables.update(m, reqs)
+        else:
+            for r in reqs.tolist():
+                m.append_slot(r)
+            np.array([m.block_table(r) + [-1] * (maxb - len(m.block_table(r))) for r in reqs.tolist()], np.int32)
+    t2 = time.perf_counter()
+    return t1 - t0, (t2 - t1) / decode_steps, len(prompts)
+
+
+def run_block_manager(args) -> dict:
+    from oracle import block_pool as obp
+    from paged_kv_cache_69_gb300 import block_manager as hbm
+    n_req, bs, steps = 1024, 16, max(args.steps, 10)
+    prompts = _bm_trace(n_req, bs, 2)
+    nb = sum(-(-(len(p) + steps) // bs) for p in prompts) + 64
+    # warm-up, then the timed run
+    _bm_run(lambda: hbm.HostBlockManager(nb, bs), hbm.block_hashes, prompts, bs, 2)
+    admit, step, n = _bm_run(lambda: hbm.HostBlockManager(nb, bs), hbm.block_hashes, prompts, bs, steps)
+    # the oracle on a bounded sample of the same trace
+    o_admit, o_step, o_n = _bm_run(lambda: obp.BlockManager(nb, bs), obp.chain_hashes, prompts, bs, 5,
+                                   reqs_cap=256)
+    return {"metric": "host block manager: decode step (one token for each of 1024 requests + block tables)",
+            "component": "block_manager", "value": step * 1e6, "unit": "us", "higher_is_better": False,
+            "steps": steps, "config": {"workload": "short mix prompts behind 4 shared 256-token system prompts",
+                                       "requests": n, "block_size": bs, "num_blocks": nb},
+            "admit_us_per_request": admit / n * 1e6, "tokens_per_s": n / step,
+            "cpu_baseline": {"value": o_step * (n / o_n) * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+                             "sample": f"first {o_n} requests, 5 steps, scaled to {n} requests"}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,7 +456,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--component", choices=["decode", "block_manager"], default="decode",
+                    help="block_manager: time the host allocator instead of the GPU path")
     args = ap.parse_args()
+    if args.component == "block_manager":
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_block_manager(args)))
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

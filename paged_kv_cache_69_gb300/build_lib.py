@@ -79,5 +79,36 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), csrc: str 
     return lib
 
 
+# ---------------------------------------------------------------------------
+# host library (libpa_host.so: the block manager, plain C++, no CUDA)
+# ---------------------------------------------------------------------------
+HOST_SRC = os.path.join(HERE, "host")
+HOST_LIB = os.path.join(HERE, "libpa_host.so")
+
+
+def _host_deps():
+    return sorted(glob.glob(os.path.join(HOST_SRC, "*.cpp"))) + \
+        [os.path.join(ROOT, "include", "pa_block_manager.h"), os.path.abspath(__file__)]
+
+
+def build_host(force: bool = False) -> str:
+    """Compile host/*.cpp with the system C++ compiler into libpa_host.so."""
+    if not force and os.path.exists(HOST_LIB) and \
+            all(os.path.getmtime(d) <= os.path.getmtime(HOST_LIB) for d in _host_deps()):
+        return HOST_LIB
+    cxx = os.environ.get("CXX") or shutil.which("g++") or shutil.which("c++")
+    if not cxx:
+        raise RuntimeError("no C++ compiler found")
+    tmp = HOST_LIB + f".tmp{os.getpid()}"
+    cmd = [cxx, "-O2", "-std=c++17", "-fPIC", "-shared", "-Wall", "-Wextra",
+           *sorted(glob.glob(os.path.join(HOST_SRC, "*.cpp"))), "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"host build failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, HOST_LIB)
+    return HOST_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build_host(force="--force" in sys.argv))
