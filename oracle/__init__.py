@@ -26,9 +26,9 @@ import numpy as np
 from . import build as _build
 
 # element type codes of the library's C interface
-F32, F16, BF16, FP8_E4M3 = 0, 1, 2, 3
-DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16, "fp8_e4m3": FP8_E4M3}
-ELEM_BYTES = {F32: 4, F16: 2, BF16: 2, FP8_E4M3: 1}
+F32, F16, BF16, FP8_E4M3, FP8_E5M2 = 0, 1, 2, 3, 4
+DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16, "fp8_e4m3": FP8_E4M3, "fp8_e5m2": FP8_E5M2}
+ELEM_BYTES = {F32: 4, F16: 2, BF16: 2, FP8_E4M3: 1, FP8_E5M2: 1}
 
 _lib = None
 
@@ -51,6 +51,12 @@ def lib():
         L.pao_decode_array.argtypes = [c_void_p, c_void_p, c_int, ctypes.c_int64]
         L.pao_encode_e4m3_array.restype = None
         L.pao_encode_e4m3_array.argtypes = [c_void_p, c_void_p, ctypes.c_int64, c_float]
+        L.pao_e5m2_to_double.restype = c_double
+        L.pao_e5m2_to_double.argtypes = [ctypes.c_uint8]
+        L.pao_float_to_e5m2_satfinite.restype = ctypes.c_uint8
+        L.pao_float_to_e5m2_satfinite.argtypes = [c_float]
+        L.pao_encode_e5m2_array.restype = None
+        L.pao_encode_e5m2_array.argtypes = [c_void_p, c_void_p, ctypes.c_int64, c_float]
         L.pao_gather.restype = c_int
         L.pao_gather.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                  c_int, c_int, c_int, c_double]
@@ -85,7 +91,7 @@ def as_raw(x) -> np.ndarray:
             t = x.detach().cpu().contiguous()
             if t.dtype == torch.bfloat16:
                 t = t.view(torch.int16)
-            elif t.dtype == torch.float8_e4m3fn:
+            elif t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
                 t = t.view(torch.uint8)
             a = t.numpy()
             if a.dtype == np.int16:
@@ -110,6 +116,13 @@ def encode_e4m3(x: np.ndarray, scale: float = 1.0) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty(x.size, dtype=np.uint8)
     lib().pao_encode_e4m3_array(_ptr(out), _ptr(x), x.size, float(scale))
+    return out.reshape(x.shape)
+
+
+def encode_e5m2(x: np.ndarray, scale: float = 1.0) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.size, dtype=np.uint8)
+    lib().pao_encode_e5m2_array(_ptr(out), _ptr(x), x.size, float(scale))
     return out.reshape(x.shape)
 
 
@@ -191,6 +204,22 @@ def reshape_and_cache(k_cache: np.ndarray, v_cache: np.ndarray, kv_dtype: int,
     if rc < 0:
         raise ValueError(f"oracle reshape_and_cache failed with status {rc}")
     return rc
+
+
+def swap_blocks(dst_k: np.ndarray, dst_v: np.ndarray, src_k: np.ndarray, src_v: np.ndarray,
+                block_mapping: np.ndarray) -> int:
+    """Block copies between two pools of one block shape (swap-out of a
+    preempted request's KV to CPU memory and swap-in back,
+    "kv-cache-memory-core", preemption section): dst[d] = src[s] for every
+    pair (s, d) whose ids lie in their pools.  Returns the pairs skipped."""
+    skipped = 0
+    for s, d in np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2).tolist():
+        if 0 <= s < src_k.shape[0] and 0 <= d < dst_k.shape[0]:
+            dst_k[d] = src_k[s]
+            dst_v[d] = src_v[s]
+        else:
+            skipped += 1
+    return skipped
 
 
 def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, kv_dtype: int,

@@ -28,10 +28,12 @@
  *    ("vLLM intro part 2", section 4.2 key formulas; "kv-cache-memory-core",
  *    section 3, attention read pseudo-code).
  *  - fp8 KV: quantise on write, dequantise on read
- *    ("kv-cache-memory-core", section 4.4), E4M3 with 3 mantissa bits
- *    ("vLLM intro part 2", section 7).  The codec below is written from the
- *    OCP FP8 E4M3 definition (bias 7, no infinities, S.1111.111 is NaN,
- *    largest finite 448); the per-tensor scale is an input.
+ *    ("kv-cache-memory-core", section 4.4), E4M3 with 3 mantissa bits or
+ *    E5M2 with 2 ("vLLM intro part 2", section 7, which names both).  The
+ *    codecs below are written from the OCP FP8 definitions (E4M3: bias 7, no
+ *    infinities, S.1111.111 is NaN, largest finite 448; E5M2: bias 15,
+ *    IEEE-like infinities and NaNs, largest finite 57344); the per-tensor
+ *    scale is an input.
  *  - copy_blocks: copy-on-write copies the whole content of a shared block
  *    into a fresh one before the write ("vLLM intro part 2", section 5;
  *    aibook "显存与 KV 缓存", the five copy-on-write steps).
@@ -46,7 +48,9 @@
 #include <string.h>
 
 /* Element type codes, as the library's C interface numbers them. */
-enum { PAO_F32 = 0, PAO_F16 = 1, PAO_BF16 = 2, PAO_FP8_E4M3 = 3 };
+enum { PAO_F32 = 0, PAO_F16 = 1, PAO_BF16 = 2, PAO_FP8_E4M3 = 3, PAO_FP8_E5M2 = 4 };
+
+static int pao_is_fp8(int dtype) { return dtype == PAO_FP8_E4M3 || dtype == PAO_FP8_E5M2; }
 
 /* Error codes returned by the oracle (not device flags). */
 enum { PAO_OK = 0, PAO_BAD_ARG = -1, PAO_BAD_BLOCK = -2 };
@@ -57,6 +61,7 @@ static size_t pao_elem_bytes(int dtype) {
         case PAO_F16: return 2;
         case PAO_BF16: return 2;
         case PAO_FP8_E4M3: return 1;
+        case PAO_FP8_E5M2: return 1;
         default: return 0;
     }
 }
@@ -140,6 +145,52 @@ uint8_t pao_float_to_e4m3_satfinite(float x) {
     return sign | (uint8_t)code;
 }
 
+/* OCP FP8 E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits,
+ * IEEE-like: exponent 11111 is infinity (fraction 0) or NaN; largest finite
+ * value 1.75 * 2^15 = 57344; subnormals are m * 2^-16. */
+double pao_e5m2_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1f;
+    int m = b & 3;
+    double v;
+    if (e == 31) {
+        if (m != 0) return NAN;
+        v = INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)m, -16);
+    } else {
+        v = ldexp((double)(4 + m), e - 17);  /* (1 + m/4) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* float -> E5M2 with round-to-nearest-even and saturation of overflow and
+ * infinities to the largest finite value (+-57344); NaN maps to 0x7F. */
+uint8_t pao_float_to_e5m2_satfinite(float x) {
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 57344.0) return sign | 0x7b;
+    unsigned code;
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: value = m * 2^-16, m in [0, 4]; m == 4 is the
+         * smallest normal (code 0x04). */
+        code = (unsigned)pao_round_half_even(a * 65536.0);
+    } else {
+        int ex;
+        double fr = frexp(a, &ex);        /* a = fr * 2^ex, fr in [0.5, 1) */
+        int E = ex - 1;
+        double r = pao_round_half_even(fr * 8.0);   /* (1 + f/4) * 4 in [4, 8] */
+        code = (unsigned)((E + 15) << 2) + (unsigned)(r - 4.0);   /* r == 8 carries */
+    }
+    if (code > 0x7b) code = 0x7b;
+    return sign | (uint8_t)code;
+}
+
+static uint8_t pao_float_to_fp8(int dtype, float x) {
+    return dtype == PAO_FP8_E5M2 ? pao_float_to_e5m2_satfinite(x) : pao_float_to_e4m3_satfinite(x);
+}
+
 /* Read element idx of a typed array as an exact double. */
 static double pao_load(const void* base, int dtype, size_t idx) {
     switch (dtype) {
@@ -147,6 +198,7 @@ static double pao_load(const void* base, int dtype, size_t idx) {
         case PAO_F16: return pao_f16_to_double(((const uint16_t*)base)[idx]);
         case PAO_BF16: return pao_bf16_to_double(((const uint16_t*)base)[idx]);
         case PAO_FP8_E4M3: return pao_e4m3_to_double(((const uint8_t*)base)[idx]);
+        case PAO_FP8_E5M2: return pao_e5m2_to_double(((const uint8_t*)base)[idx]);
         default: return NAN;
     }
 }
@@ -158,6 +210,10 @@ void pao_decode_array(double* out, const void* in, int dtype, int64_t n) {
 
 void pao_encode_e4m3_array(uint8_t* out, const float* in, int64_t n, float scale) {
     for (int64_t i = 0; i < n; ++i) out[i] = pao_float_to_e4m3_satfinite(in[i] / scale);
+}
+
+void pao_encode_e5m2_array(uint8_t* out, const float* in, int64_t n, float scale) {
+    for (int64_t i = 0; i < n; ++i) out[i] = pao_float_to_e5m2_satfinite(in[i] / scale);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -175,7 +231,7 @@ int pao_gather(double* out, const void* cache, int dtype, const int32_t* bt_row,
         size_t row = (((size_t)blk * block_size + off) * num_kv_heads + g) * head_dim;
         for (int d = 0; d < head_dim; ++d) {
             double v = pao_load(cache, dtype, row + d);
-            if (dtype == PAO_FP8_E4M3) v *= elem_scale;
+            if (pao_is_fp8(dtype)) v *= elem_scale;
             out[(size_t)t * head_dim + d] = v;
         }
     }
@@ -280,7 +336,7 @@ static void pao_store(void* cache, int kv_dtype, size_t idx, const void* src,
     } else {
         /* only fp8 caches accept another source type */
         float x = (float)pao_load(src, src_dtype, sidx);  /* exact widening */
-        ((uint8_t*)cache)[idx] = pao_float_to_e4m3_satfinite(x / scale);
+        ((uint8_t*)cache)[idx] = pao_float_to_fp8(kv_dtype, x / scale);
     }
 }
 
@@ -289,7 +345,7 @@ int pao_reshape_and_cache(void* k_cache, void* v_cache, int kv_dtype,
                           const int64_t* slot_mapping, int num_tokens,
                           int num_kv_heads, int head_dim, int block_size,
                           int num_blocks, float k_scale, float v_scale) {
-    if (kv_dtype != src_dtype && kv_dtype != PAO_FP8_E4M3) return PAO_BAD_ARG;
+    if (kv_dtype != src_dtype && !pao_is_fp8(kv_dtype)) return PAO_BAD_ARG;
     int skipped = 0;
     int64_t nslots = (int64_t)num_blocks * block_size;
     size_t row = (size_t)num_kv_heads * head_dim;
