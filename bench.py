@@ -53,6 +53,7 @@ def make_workload(name: str, seed: int, device: str):
         "prefix_share_cow_fp16": lambda: inputs.prefix_share_fp16(seed=seed + 2, prompt_len=2040, gen_device=gd),
         "long_ctx_bf16": lambda: inputs.long_ctx("bf16", seed=seed + 3, gen_device=gd),
         "long_ctx_fp8": lambda: inputs.long_ctx("fp8_e4m3", seed=seed + 3, gen_device=gd),
+        "long_ctx_fp8_e5m2": lambda: inputs.long_ctx("fp8_e5m2", seed=seed + 3, gen_device=gd),
         "tiny_fp32": lambda: inputs.tiny_fp32(seed=seed - 1),
     }
     return table[name]()

@@ -3,7 +3,9 @@
  *
  * The library implements the data-parallel hot path of paged KV caching:
  *   pa_reshape_and_cache  write new tokens' K/V into pool slots,
- *   pa_copy_blocks        copy-on-write of shared blocks,
+ *   pa_copy_blocks        copy-on-write of shared blocks (one layer, or
+ *                         all layers: pa_copy_blocks_layers),
+ *   pa_swap_blocks        block copies between a device and a host pool,
  *   pa_decode             one decode step of attention over a paged pool.
  *
  * Layouts (row-major, innermost last):
@@ -33,10 +35,10 @@
  * *err_flag (if err_flag is non-null); kernels never trap.  Identical inputs
  * give bit-identical outputs (no floating-point atomics).
  *
- * Supported shapes: head_dim 64 or 128; block_size 8, 16 or 32;
+ * Supported shapes: head_dim 64 or 128; block_size 8, 16, 32, 64 or 128;
  * num_q_heads a multiple of num_kv_heads; num_kv_heads <= 256.
  * Element types: f32 caches need f32 q; f16/bf16 caches need q of the same
- * type; fp8-e4m3 caches take f16 or bf16 q (head_dim 128 only).
+ * type; fp8 caches (e4m3 or e5m2) take f16 or bf16 q (head_dim 128 only).
  */
 #ifndef PA_H
 #define PA_H
@@ -61,7 +63,8 @@ typedef enum {
     PA_F32 = 0,
     PA_F16 = 1,
     PA_BF16 = 2,
-    PA_FP8_E4M3 = 3           /* OCP E4M3 (finite-only, max 448), one byte */
+    PA_FP8_E4M3 = 3,          /* OCP E4M3 (finite-only, max 448), one byte */
+    PA_FP8_E5M2 = 4           /* OCP E5M2 (IEEE-like inf/NaN, max 57344), one byte */
 } pa_dtype;
 
 /* Bits OR-ed into *err_flag by device code. */
@@ -209,6 +212,36 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype kv_dtype,
                          const int64_t* block_mapping, int num_pairs,
                          int num_kv_heads, int head_dim, int block_size,
                          int num_blocks, int32_t* err_flag, cudaStream_t stream);
+
+/*
+ * pa_copy_blocks_layers -- pa_copy_blocks for every layer of a model in one
+ * launch: the same pairs are copied in each of the num_layers K and V pools.
+ * k_caches and v_caches are HOST arrays of num_layers device pointers (pools
+ * of identical shape, 16-byte aligned); num_layers <= 256.
+ */
+pa_status pa_copy_blocks_layers(void* const* k_caches, void* const* v_caches, int num_layers,
+                                pa_dtype kv_dtype, const int64_t* block_mapping, int num_pairs,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                int32_t* err_flag, cudaStream_t stream);
+
+/*
+ * pa_swap_blocks -- block-granular swap between two pools of the same block
+ * shape, typically a device pool and a host pool (preemption by swapping a
+ * request's KV out to CPU memory and back in, "kv-cache-memory-core", the
+ * preemption section: swap keeps the progress at the cost of CPU memory and
+ * interconnect bandwidth).  For each pair p the K and V block
+ * block_mapping[2p] of the source pool are copied to block
+ * block_mapping[2p+1] of the destination pool.  Either pool may be host
+ * memory the device can address (pinned with cudaHostAlloc / cudaMallocHost,
+ * or cudaHostRegister-ed); block_mapping must be device-accessible.  Ids
+ * outside their pool are skipped with PA_ERRBIT_BAD_PAIR.  The two pools must
+ * not overlap.  A kernel performs the copy, so swaps of many scattered blocks
+ * cost one launch, not one transfer per block.
+ */
+pa_status pa_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks, const void* src_k,
+                         const void* src_v, int src_num_blocks, pa_dtype kv_dtype,
+                         const int64_t* block_mapping, int num_pairs, int num_kv_heads,
+                         int head_dim, int block_size, int32_t* err_flag, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -18,18 +18,19 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpa.so")
 
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = 0, 1, 2, 3, 4
 PA_OK = 0
 ERRBIT_BAD_BLOCK, ERRBIT_BAD_SLOT, ERRBIT_BAD_PAIR, ERRBIT_SEQ_TOO_LONG, ERRBIT_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 
 # entry points declared in include/pa.h
 EXPORTED = ("pa_status_string", "pa_last_error_detail", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_simt", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks")
+            "pa_decode_simt", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks",
+            "pa_copy_blocks_layers", "pa_swap_blocks")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _DTYPE_CODE = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16,
-               torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: PA_FP8_E4M3}
-_NAME_CODE = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3}
+               torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: PA_FP8_E4M3, torch.float8_e5m2: PA_FP8_E5M2}
+_NAME_CODE = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "fp8_e4m3": PA_FP8_E4M3, "fp8_e5m2": PA_FP8_E5M2}
 
 
 class PaError(RuntimeError):
@@ -67,6 +68,10 @@ def _configure(L):
                                        c_int, c_float, c_float, vp, vp]
     L.pa_copy_blocks.restype = c_int
     L.pa_copy_blocks.argtypes = [vp, vp, c_int, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]
+    L.pa_copy_blocks_layers.restype = c_int
+    L.pa_copy_blocks_layers.argtypes = [vp, vp, c_int, c_int, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]
+    L.pa_swap_blocks.restype = c_int
+    L.pa_swap_blocks.argtypes = [vp, vp, c_int, vp, vp, c_int, c_int, vp, c_int, c_int, c_int, c_int, vp, vp]
     return L
 
 
@@ -207,3 +212,45 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: 
     P = block_mapping.numel() // 2
     _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _code(k_cache, kv_dtype), _ptr(block_mapping),
                                 P, Hkv, D, bs, NB, _ptr(err_flag), _stream(stream)))
+
+
+def pa_copy_blocks_layers(k_caches, v_caches, block_mapping: torch.Tensor, kv_dtype=None, *,
+                          err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pa_copy_blocks over lists of per-layer pools of one shape."""
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("k_caches and v_caches must be equal-length non-empty lists")
+    _dev(*k_caches, *v_caches, block_mapping, err_flag)
+    NB, bs, Hkv, D = k_caches[0].shape
+    for t in list(k_caches) + list(v_caches):
+        if tuple(t.shape) != (NB, bs, Hkv, D) or t.dtype != k_caches[0].dtype:
+            raise ValueError("all pools must have one shape and dtype")
+    if block_mapping.dtype != torch.int64 or (block_mapping.numel() and block_mapping.shape[-1] != 2):
+        raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    L = len(k_caches)
+    kp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_caches])
+    vp_ = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
+    _check(lib().pa_copy_blocks_layers(kp, vp_, L, _code(k_caches[0], kv_dtype), _ptr(block_mapping),
+                                       block_mapping.numel() // 2, Hkv, D, bs, NB, _ptr(err_flag),
+                                       _stream(stream)))
+
+
+def pa_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor,
+                   block_mapping: torch.Tensor, kv_dtype=None, *, err_flag: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Copy blocks src -> dst between two pools; either may be pinned host
+    memory (torch pin_memory()), block_mapping must be on the device."""
+    for t in (dst_k, dst_v, src_k, src_v):
+        if not t.is_contiguous():
+            raise ValueError("pools must be contiguous")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("pools must be device memory or pinned host memory")
+    _dev(block_mapping, err_flag)
+    NBd, bs, Hkv, D = dst_k.shape
+    NBs = src_k.shape[0]
+    if tuple(src_k.shape[1:]) != (bs, Hkv, D) or dst_v.shape != dst_k.shape or src_v.shape != src_k.shape:
+        raise ValueError("pools must share the block shape")
+    if block_mapping.dtype != torch.int64 or (block_mapping.numel() and block_mapping.shape[-1] != 2):
+        raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    _check(lib().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), NBd, _ptr(src_k), _ptr(src_v), NBs,
+                                _code(dst_k, kv_dtype), _ptr(block_mapping), block_mapping.numel() // 2,
+                                Hkv, D, bs, _ptr(err_flag), _stream(stream)))

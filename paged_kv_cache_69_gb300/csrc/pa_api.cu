@@ -154,7 +154,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     if (!valid_dtype(q_dtype) || !valid_dtype(kv_dtype)) return fail(PA_ERR_INVALID_ARG, "decode: unknown dtype");
     if (Hq % Hkv != 0) return fail(PA_ERR_INVALID_ARG, "decode: num_q_heads must be a multiple of num_kv_heads");
     if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "decode: head_dim must be 64 or 128");
-    if (bs != 8 && bs != 16 && bs != 32) return fail(PA_ERR_UNSUPPORTED, "decode: block_size must be 8, 16 or 32");
+    if (bs != 8 && bs != 16 && bs != 32 && bs != 64 && bs != 128)
+        return fail(PA_ERR_UNSUPPORTED, "decode: block_size must be 8, 16, 32, 64 or 128");
     if (Hkv > 256) return fail(PA_ERR_UNSUPPORTED, "decode: num_kv_heads must be <= 256");
     if (partition_tokens < 0 || partition_tokens % 16 != 0)
         return fail(PA_ERR_INVALID_ARG, "decode: partition_tokens must be 0 or a positive multiple of 16");
@@ -162,7 +163,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         return fail(PA_ERR_UNSUPPORTED, "decode: pool or table too large for 32-bit row coordinates");
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "decode: q, out, k_cache and v_cache must be 16-byte aligned");
-    if (kv_dtype == PA_FP8_E4M3) {
+    if (is_fp8(kv_dtype)) {
         if (q_dtype != PA_F16 && q_dtype != PA_BF16)
             return fail(PA_ERR_UNSUPPORTED, "decode: an fp8 cache needs f16 or bf16 queries");
         if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite_host(k_scale) || !isfinite_host(v_scale))
@@ -259,8 +260,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.bar_off = (p.simtq_off + simtq + 15u) & ~15u;
     const size_t smem = 1024 + p.bar_off + extras;
     const float log2e = 1.4426950408889634f;
-    p.qk_scale = scale * log2e * (kv_dtype == PA_FP8_E4M3 ? k_scale : 1.f);
-    p.v_scale = kv_dtype == PA_FP8_E4M3 ? v_scale : 1.f;
+    p.qk_scale = scale * log2e * (is_fp8(kv_dtype) ? k_scale : 1.f);
+    p.v_scale = is_fp8(kv_dtype) ? v_scale : 1.f;
 
     // workspace
     const size_t need = workspace_bytes_for(B, Hq, D, MB * bs, partition_tokens, dev.sms);

@@ -10,8 +10,12 @@
 // CUDA's saturating round-to-nearest-even E4M3 conversion.
 //
 // copy_blocks: copy-on-write copies of whole blocks ("vLLM intro part 2",
-// section 5): one CTA per (pair, K|V), 16-byte vector copies.
+// section 5), for one layer's pools or for all layers in one launch; swap:
+// the same block copy between a device pool and a host pool (preemption by
+// swapping a request's blocks out to CPU memory and back,
+// "kv-cache-memory-core", section on preemption).  16-byte vector copies.
 #include <cstdint>
+#include <cstdio>
 
 #include "pa_common.h"
 #include "pa_device.cuh"
@@ -38,9 +42,9 @@ struct Conv<X, X> {
     }
 };
 
-// any float source -> e4m3
-template <class S>
-struct Conv<S, FP8T> {
+// any float source -> e4m3 or e5m2
+template <class S, class F8>
+struct ConvFp8 {
     static __device__ __forceinline__ void run(const uint8_t* src, uint8_t* dst, float scale) {
         float x[VEC];
         if constexpr (S::code == PA_F32) {
@@ -56,17 +60,24 @@ struct Conv<S, FP8T> {
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int k = 0; k < VEC; ++k) {
-            const uint32_t b = static_cast<uint32_t>(
-                __nv_cvt_float_to_fp8(__fdiv_rn(x[k], scale), __NV_SATFINITE, __NV_E4M3));
+            const uint32_t b = static_cast<uint32_t>(__nv_cvt_float_to_fp8(
+                __fdiv_rn(x[k], scale), __NV_SATFINITE, F8::code == PA_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3));
             if (k < 4) lo |= b << (8 * k); else hi |= b << (8 * (k - 4));
         }
         reinterpret_cast<uint2*>(dst)[0] = make_uint2(lo, hi);
     }
 };
 
+template <class S> struct Conv<S, FP8T> : ConvFp8<S, FP8T> {};
+template <class S> struct Conv<S, E5M2T> : ConvFp8<S, E5M2T> {};
+
 // an already-quantised source: move bytes
-template <>
-struct Conv<FP8T, FP8T> {
+template <> struct Conv<FP8T, FP8T> {
+    static __device__ __forceinline__ void run(const uint8_t* src, uint8_t* dst, float) {
+        reinterpret_cast<uint2*>(dst)[0] = reinterpret_cast<const uint2*>(src)[0];
+    }
+};
+template <> struct Conv<E5M2T, E5M2T> {
     static __device__ __forceinline__ void run(const uint8_t* src, uint8_t* dst, float) {
         reinterpret_cast<uint2*>(dst)[0] = reinterpret_cast<const uint2*>(src)[0];
     }
@@ -96,20 +107,77 @@ reshape_and_cache_kernel(uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
     }
 }
 
+// Whole-block copies between two pools of the same shape, for every layer
+// and both K and V: copy-on-write inside one pool (source pool = destination
+// pool) and swapping blocks between a device pool and a host pool the
+// device can address.  One CTA per (pair, layer, K|V).
+constexpr int MAX_LAYERS = 256;
+struct BlockCopyArgs {
+    uint8_t* dst[2][MAX_LAYERS];           // [K|V][layer]
+    const uint8_t* src[2][MAX_LAYERS];
+    const int64_t* pairs;                  // (src block, dst block) per pair
+    int64_t block_bytes;
+    int src_blocks, dst_blocks;
+    int32_t* err;
+};
+
 __global__ void __launch_bounds__(256)
-copy_blocks_kernel(uint8_t* __restrict__ kc, uint8_t* __restrict__ vc, const int64_t* __restrict__ pairs,
-                   int64_t block_bytes, int num_blocks, int32_t* err) {
-    const int p = blockIdx.x;
-    const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
-    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
-        if (threadIdx.x == 0 && blockIdx.y == 0) raise_flag(err, PA_ERRBIT_BAD_PAIR);
+block_copy_kernel(const __grid_constant__ BlockCopyArgs a) {
+    const int p = blockIdx.x, l = blockIdx.y, kv = blockIdx.z;
+    const int64_t src = a.pairs[2 * static_cast<int64_t>(p)], dst = a.pairs[2 * static_cast<int64_t>(p) + 1];
+    if (src < 0 || src >= a.src_blocks || dst < 0 || dst >= a.dst_blocks) {
+        if (threadIdx.x == 0 && l == 0 && kv == 0) raise_flag(a.err, PA_ERRBIT_BAD_PAIR);
         return;
     }
-    uint8_t* base = blockIdx.y == 0 ? kc : vc;
-    const uint4* s = reinterpret_cast<const uint4*>(base + src * block_bytes);
-    uint4* d = reinterpret_cast<uint4*>(base + dst * block_bytes);
-    const int64_t n = block_bytes / 16;
+    const uint4* s = reinterpret_cast<const uint4*>(a.src[kv][l] + src * a.block_bytes);
+    uint4* d = reinterpret_cast<uint4*>(a.dst[kv][l] + dst * a.block_bytes);
+    const int64_t n = a.block_bytes / 16;
     for (int64_t k = threadIdx.x; k < n; k += blockDim.x) d[k] = s[k];
+}
+
+// Validates and launches a block copy over num_layers pools.
+static pa_status launch_block_copy(const char* who, void* const* dst_k, void* const* dst_v,
+                                   const void* const* src_k, const void* const* src_v, int num_layers,
+                                   pa_dtype kv_dtype, const int64_t* pairs, int num_pairs, int num_kv_heads,
+                                   int head_dim, int block_size, int src_blocks, int dst_blocks,
+                                   int32_t* err_flag, cudaStream_t stream) {
+    char msg[128];
+    auto bad = [&](pa_status st, const char* what) {
+        std::snprintf(msg, sizeof msg, "%s: %s", who, what);
+        return fail(st, msg);
+    };
+    if (num_pairs < 0 || num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        src_blocks <= 0 || dst_blocks <= 0)
+        return bad(PA_ERR_INVALID_ARG, "sizes must be positive (num_pairs >= 0)");
+    if (num_layers > MAX_LAYERS) return bad(PA_ERR_UNSUPPORTED, "more than 256 layers");
+    if (!valid_dtype(kv_dtype)) return bad(PA_ERR_INVALID_ARG, "unknown dtype");
+    if (num_pairs == 0) return PA_OK;
+    if (!pairs || !dst_k || !dst_v || !src_k || !src_v) return bad(PA_ERR_INVALID_ARG, "null pointer");
+    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * dtype_bytes(kv_dtype);
+    if (block_bytes % 16 != 0) return bad(PA_ERR_UNSUPPORTED, "block bytes must be a multiple of 16");
+    BlockCopyArgs a{};
+    for (int l = 0; l < num_layers; ++l) {
+        if (!dst_k[l] || !dst_v[l] || !src_k[l] || !src_v[l]) return bad(PA_ERR_INVALID_ARG, "null pool pointer");
+        if (!aligned16(dst_k[l]) || !aligned16(dst_v[l]) || !aligned16(src_k[l]) || !aligned16(src_v[l]))
+            return bad(PA_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+        a.dst[0][l] = static_cast<uint8_t*>(dst_k[l]);
+        a.dst[1][l] = static_cast<uint8_t*>(dst_v[l]);
+        a.src[0][l] = static_cast<const uint8_t*>(src_k[l]);
+        a.src[1][l] = static_cast<const uint8_t*>(src_v[l]);
+    }
+    a.pairs = pairs;
+    a.block_bytes = block_bytes;
+    a.src_blocks = src_blocks;
+    a.dst_blocks = dst_blocks;
+    a.err = err_flag;
+    dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(num_layers), 2);
+    block_copy_kernel<<<grid, 256, 0, stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        std::snprintf(msg, sizeof msg, "%s launch", who);
+        return fail_cuda(msg, e);
+    }
+    return PA_OK;
 }
 
 template <class S, class Dt>
@@ -150,7 +218,17 @@ extern "C" pa_status pa_reshape_and_cache(void* k_cache, void* v_cache, pa_dtype
     const int64_t nslots = static_cast<int64_t>(num_blocks) * block_size;
     cudaError_t e;
     const int re = static_cast<int>(row_elems);
-    if (kv_dtype == PA_FP8_E4M3) {
+    if (kv_dtype == PA_FP8_E5M2) {
+        if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite_host(k_scale) || !isfinite_host(v_scale))
+            return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: fp8 scales must be finite and > 0");
+        switch (src_dtype) {
+            case PA_F32: e = launch_rc<F32T, E5M2T>(k_cache, v_cache, key, value, slot_mapping, num_tokens, re, block_size, nslots, k_scale, v_scale, err_flag, stream); break;
+            case PA_F16: e = launch_rc<F16T, E5M2T>(k_cache, v_cache, key, value, slot_mapping, num_tokens, re, block_size, nslots, k_scale, v_scale, err_flag, stream); break;
+            case PA_BF16: e = launch_rc<BF16T, E5M2T>(k_cache, v_cache, key, value, slot_mapping, num_tokens, re, block_size, nslots, k_scale, v_scale, err_flag, stream); break;
+            case PA_FP8_E5M2: e = launch_rc<E5M2T, E5M2T>(k_cache, v_cache, key, value, slot_mapping, num_tokens, re, block_size, nslots, 1.f, 1.f, err_flag, stream); break;
+            default: return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: e5m2 cache needs an f32, f16, bf16 or e5m2 source");
+        }
+    } else if (kv_dtype == PA_FP8_E4M3) {
         if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite_host(k_scale) || !isfinite_host(v_scale))
             return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: fp8 scales must be finite and > 0");
         switch (src_dtype) {
@@ -177,20 +255,37 @@ extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype kv_dt
                                     int num_kv_heads, int head_dim, int block_size,
                                     int num_blocks, int32_t* err_flag, cudaStream_t stream) {
     clear_error();
-    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
-        return fail(PA_ERR_INVALID_ARG, "copy_blocks: sizes must be positive (num_pairs >= 0)");
-    if (num_pairs == 0) return PA_OK;
-    if (!k_cache || !v_cache || !block_mapping)
+    void* k[1] = {k_cache};
+    void* v[1] = {v_cache};
+    const void* ks[1] = {k_cache};
+    const void* vs[1] = {v_cache};
+    if (num_pairs > 0 && (!k_cache || !v_cache || !block_mapping))
         return fail(PA_ERR_INVALID_ARG, "copy_blocks: null pointer");
-    if (!valid_dtype(kv_dtype)) return fail(PA_ERR_INVALID_ARG, "copy_blocks: unknown dtype");
-    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * dtype_bytes(kv_dtype);
-    if (block_bytes % 16 != 0)
-        return fail(PA_ERR_UNSUPPORTED, "copy_blocks: block bytes must be a multiple of 16");
-    if (!aligned16(k_cache) || !aligned16(v_cache))
-        return fail(PA_ERR_INVALID_ARG, "copy_blocks: caches must be 16-byte aligned");
-    dim3 grid(static_cast<unsigned>(num_pairs), 2);
-    copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
-                                                 block_mapping, block_bytes, num_blocks, err_flag);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? PA_OK : fail_cuda("copy_blocks launch", e);
+    return launch_block_copy("copy_blocks", k, v, ks, vs, 1, kv_dtype, block_mapping, num_pairs, num_kv_heads,
+                             head_dim, block_size, num_blocks, num_blocks, err_flag, stream);
+}
+
+extern "C" pa_status pa_copy_blocks_layers(void* const* k_caches, void* const* v_caches, int num_layers,
+                                           pa_dtype kv_dtype, const int64_t* block_mapping, int num_pairs,
+                                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                           int32_t* err_flag, cudaStream_t stream) {
+    clear_error();
+    return launch_block_copy("copy_blocks_layers", k_caches, v_caches,
+                             reinterpret_cast<const void* const*>(k_caches),
+                             reinterpret_cast<const void* const*>(v_caches), num_layers, kv_dtype,
+                             block_mapping, num_pairs, num_kv_heads, head_dim, block_size, num_blocks,
+                             num_blocks, err_flag, stream);
+}
+
+extern "C" pa_status pa_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks, const void* src_k,
+                                    const void* src_v, int src_num_blocks, pa_dtype kv_dtype,
+                                    const int64_t* block_mapping, int num_pairs, int num_kv_heads,
+                                    int head_dim, int block_size, int32_t* err_flag, cudaStream_t stream) {
+    clear_error();
+    void* dk[1] = {dst_k};
+    void* dv[1] = {dst_v};
+    const void* sk[1] = {src_k};
+    const void* sv[1] = {src_v};
+    return launch_block_copy("swap_blocks", dk, dv, sk, sv, 1, kv_dtype, block_mapping, num_pairs, num_kv_heads,
+                             head_dim, block_size, src_num_blocks, dst_num_blocks, err_flag, stream);
 }

@@ -327,11 +327,12 @@ template <class KV, class QT, int D, bool TC, int CT>
 struct DecodeKernel {
     using KT = typename KV::T;
     using QE = typename QT::T;
-    static constexpr bool FP8 = (KV::code == PA_FP8_E4M3);
+    static constexpr bool FP8 = (KV::bytes == 1);             // e4m3 or e5m2
     // 32-token chunks are the native-e4m3 tensor-core variant (fp8 operands,
     // m16n8k32); every other variant runs 16-token chunks.
     static constexpr bool NATIVE8 = (CT == 32);
-    static_assert(CT == 16 || (CT == 32 && FP8 && TC && D == 128), "32-token chunks: fp8 tensor-core path only");
+    static_assert(CT == 16 || (CT == 32 && KV::code == PA_FP8_E4M3 && TC && D == 128),
+                  "32-token chunks: e4m3 tensor-core path only");
     static constexpr int MAXB = CT / 8;       // TMA boxes per chunk at the smallest block size
     static constexpr bool MMA_BF16 = (KV::code == PA_BF16);   // fp8 runs in f16
     static constexpr int NT = D / 8;          // 8-wide output column tiles
@@ -683,10 +684,10 @@ struct DecodeKernel {
                 for (int ks = 0; ks < KS; ks += 2) {
                     uint32_t r0, r1, r2, r3;    // (tile0,ks) (tile0,ks+1) (tile1,ks) (tile1,ks+1)
                     ldsm_x4(kb + lay.chunk_addr(rbK, tokK, ks + (mi & 1)), r0, r1, r2, r3);
-                    mma_16816<false>(s[0], qa[ks], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
-                    mma_16816<false>(s2[0], qa[ks + 1], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
-                    mma_16816<false>(s[1], qa[ks], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
-                    mma_16816<false>(s2[1], qa[ks + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+                    mma_16816<false>(s[0], qa[ks], fp8x2_to_f16x2<KV>(r0), fp8x2_to_f16x2<KV>(r0 >> 16));
+                    mma_16816<false>(s2[0], qa[ks + 1], fp8x2_to_f16x2<KV>(r1), fp8x2_to_f16x2<KV>(r1 >> 16));
+                    mma_16816<false>(s[1], qa[ks], fp8x2_to_f16x2<KV>(r2), fp8x2_to_f16x2<KV>(r2 >> 16));
+                    mma_16816<false>(s2[1], qa[ks + 1], fp8x2_to_f16x2<KV>(r3), fp8x2_to_f16x2<KV>(r3 >> 16));
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -751,10 +752,10 @@ struct DecodeKernel {
                     ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, c2 + (mi >> 1)), r0, r1, r2, r3);
                     const uint32_t x0 = __byte_perm(r0 & vk0, 0, 0x3120), x1 = __byte_perm(r1 & vk1, 0, 0x3120);
                     const uint32_t x2 = __byte_perm(r2 & vk0, 0, 0x3120), x3 = __byte_perm(r3 & vk1, 0, 0x3120);
-                    mma_16816<false>(acc[2 * c2], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
-                    mma_16816<false>(acc[2 * c2 + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
-                    mma_16816<false>(acc[2 * c2 + 2], pa, e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x3));
-                    mma_16816<false>(acc[2 * c2 + 3], pa, e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16));
+                    mma_16816<false>(acc[2 * c2], pa, fp8x2_to_f16x2<KV>(x0), fp8x2_to_f16x2<KV>(x1));
+                    mma_16816<false>(acc[2 * c2 + 1], pa, fp8x2_to_f16x2<KV>(x0 >> 16), fp8x2_to_f16x2<KV>(x1 >> 16));
+                    mma_16816<false>(acc[2 * c2 + 2], pa, fp8x2_to_f16x2<KV>(x2), fp8x2_to_f16x2<KV>(x3));
+                    mma_16816<false>(acc[2 * c2 + 3], pa, fp8x2_to_f16x2<KV>(x2 >> 16), fp8x2_to_f16x2<KV>(x3 >> 16));
                 }
             }
             // The stage's shared memory is no longer read: hand it back to
@@ -1224,7 +1225,7 @@ struct DecodeKernel {
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const uint32_t h01 = e4m3x2_to_f16x2(w[e]), h23 = e4m3x2_to_f16x2(w[e] >> 16);
+                const uint32_t h01 = fp8x2_to_f16x2<K2>(w[e]), h23 = fp8x2_to_f16x2<K2>(w[e] >> 16);
                 const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
                 const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
                 f[4 * e] = a.x; f[4 * e + 1] = a.y; f[4 * e + 2] = b.x; f[4 * e + 3] = b.y;
@@ -1239,6 +1240,7 @@ struct DecodeKernel {
             if constexpr (K2::code == PA_F32) f[c] = reinterpret_cast<const float*>(src)[c];
             else if constexpr (K2::code == PA_F16) f[c] = __half2float(reinterpret_cast<const __half*>(src)[c]);
             else if constexpr (K2::code == PA_BF16) f[c] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[c]);
+            else if constexpr (K2::code == PA_FP8_E5M2) f[c] = e5m2_to_float(src[c]);
             else f[c] = fp8_to_float(src[c]);
         }
     }

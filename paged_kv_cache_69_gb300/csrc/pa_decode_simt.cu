@@ -19,6 +19,10 @@ const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D) {
         return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, false, 16>);
     if (kv == PA_FP8_E4M3 && q == PA_BF16 && D == 128)
         return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, false, 16>);
+    if (kv == PA_FP8_E5M2 && q == PA_F16 && D == 128)
+        return reinterpret_cast<const void*>(&pa_decode_kernel<E5M2T, F16T, 128, false, 16>);
+    if (kv == PA_FP8_E5M2 && q == PA_BF16 && D == 128)
+        return reinterpret_cast<const void*>(&pa_decode_kernel<E5M2T, BF16T, 128, false, 16>);
 #undef PA_SIMT_CASE
     return nullptr;
 }

@@ -20,6 +20,10 @@ const void* decode_kernel_tc(pa_dtype kv, pa_dtype q, int D) {
         if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, true, 16>);
         if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, true, 16>);
     }
+    if (kv == PA_FP8_E5M2 && D == 128) {
+        if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<E5M2T, F16T, 128, true, 16>);
+        if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<E5M2T, BF16T, 128, true, 16>);
+    }
     return nullptr;
 }
 

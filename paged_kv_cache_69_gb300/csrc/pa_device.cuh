@@ -19,12 +19,19 @@ struct F32T  { using T = float;          static constexpr int bytes = 4; static 
 struct F16T  { using T = __half;         static constexpr int bytes = 2; static constexpr pa_dtype code = PA_F16; };
 struct BF16T { using T = __nv_bfloat16;  static constexpr int bytes = 2; static constexpr pa_dtype code = PA_BF16; };
 struct FP8T  { using T = uint8_t;        static constexpr int bytes = 1; static constexpr pa_dtype code = PA_FP8_E4M3; };
+struct E5M2T { using T = uint8_t;        static constexpr int bytes = 1; static constexpr pa_dtype code = PA_FP8_E5M2; };
 
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float fp8_to_float(uint8_t b) {
     __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+    return __half2float(__half(h));
+}
+// E5M2 is the upper byte of an f16 (same sign, exponent bias and layout).
+__device__ __forceinline__ float e5m2_to_float(uint8_t b) {
+    __half_raw h;
+    h.x = static_cast<unsigned short>(b) << 8;
     return __half2float(__half(h));
 }
 
@@ -182,6 +189,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
     __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xffffu), __NV_E4M3);
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// Two e5m2 bytes (low byte -> low half) to f16x2: each byte becomes the
+// upper byte of its half, one byte permute.  Exact.
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t two_bytes) {
+    return __byte_perm(two_bytes, 0u, 0x1404);
+}
+// The f16x2 of the two low bytes of an fp8 word, for either format.
+template <class KV>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_bytes) {
+    if constexpr (KV::code == PA_FP8_E5M2) return e5m2x2_to_f16x2(two_bytes);
+    else return e4m3x2_to_f16x2(two_bytes);
 }
 
 // D += A B with fp8-e4m3 operands and an fp32 accumulator, m16n8k32

@@ -35,9 +35,9 @@ import torch
 from .block_manager import BlockManager
 
 STORAGE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
-           "fp8_e4m3": torch.uint8}
-NAN_BITS = {"f32": 0x7FC00000, "f16": 0x7E00, "bf16": 0x7FC0, "fp8_e4m3": 0x7F}
-FP8_MAX = 448.0
+           "fp8_e4m3": torch.uint8, "fp8_e5m2": torch.float8_e5m2}
+NAN_BITS = {"f32": 0x7FC00000, "f16": 0x7E00, "bf16": 0x7FC0, "fp8_e4m3": 0x7F, "fp8_e5m2": 0x7F}
+FP8_MAX = {"fp8_e4m3": 448.0, "fp8_e5m2": 57344.0}     # largest finite value of each format
 
 
 @dataclass
@@ -83,7 +83,7 @@ class Workload:
 
     def kv_bytes(self) -> int:
         """K+V bytes over valid tokens only (each logical token counted once)."""
-        e = 1 if self.kv_dtype == "fp8_e4m3" else STORAGE[self.kv_dtype].itemsize
+        e = 1 if self.kv_dtype in FP8_MAX else STORAGE[self.kv_dtype].itemsize
         return int(self.seq_lens.sum()) * self.num_kv_heads * self.head_dim * e * 2
 
     def to(self, device) -> "Workload":
@@ -107,8 +107,8 @@ class Workload:
 # ---------------------------------------------------------------------------
 def _nan_pool(shape, kv_dtype: str, device) -> torch.Tensor:
     dt = STORAGE[kv_dtype]
-    if kv_dtype == "fp8_e4m3":
-        return torch.full(shape, NAN_BITS[kv_dtype], dtype=torch.uint8, device=device)
+    if kv_dtype in FP8_MAX:
+        return torch.full(shape, NAN_BITS[kv_dtype], dtype=torch.uint8, device=device).view(dt)
     if kv_dtype == "f32":
         return torch.full(shape, NAN_BITS[kv_dtype], dtype=torch.int32, device=device).view(dt)
     return torch.full(shape, NAN_BITS[kv_dtype], dtype=torch.int16, device=device).view(dt)
@@ -158,13 +158,14 @@ def _fill_history(wl_pool_k, wl_pool_v, block_tables, lens_old, Hkv, D, bs, dtyp
     return CacheWrite(k, v, slots.to(device))
 
 
-def _fp8_scales(writes: List[CacheWrite], new_key, new_value) -> Tuple[float, float]:
+def _fp8_scales(writes: List[CacheWrite], new_key, new_value, kv_dtype: str) -> Tuple[float, float]:
     kmax = max([float(w.key.float().abs().max()) for w in writes if w.key.numel()] +
                [float(new_key.float().abs().max())])
     vmax = max([float(w.value.float().abs().max()) for w in writes if w.value.numel()] +
                [float(new_value.float().abs().max())])
-    ks = float(torch.tensor(kmax, dtype=torch.float32) / torch.tensor(FP8_MAX, dtype=torch.float32))
-    vs = float(torch.tensor(vmax, dtype=torch.float32) / torch.tensor(FP8_MAX, dtype=torch.float32))
+    fmax = torch.tensor(FP8_MAX[kv_dtype], dtype=torch.float32)
+    ks = float(torch.tensor(kmax, dtype=torch.float32) / fmax)
+    vs = float(torch.tensor(vmax, dtype=torch.float32) / fmax)
     return ks, vs
 
 
@@ -179,7 +180,7 @@ def _plant_needles(writes_or_pool, wl: "Workload", gen, count: int, c: float):
             continue
         for g in range(wl.num_kv_heads):
             qh = wl.q[i, g * G].float()
-            kvec = (c * qh / qh.norm()).to(wl.k_cache.dtype if wl.kv_dtype != "fp8_e4m3"
+            kvec = (c * qh / qh.norm()).to(wl.k_cache.dtype if wl.kv_dtype not in FP8_MAX
                                             else STORAGE[wl.src_dtype])
             pos = torch.randint(0, n, (count,), generator=gen)
             slots = token_slots(wl.block_tables.cpu(), i, 0, n, wl.block_size)[pos]
@@ -209,7 +210,7 @@ def make_random(seq_lens: Sequence[int], *, num_q_heads: int, num_kv_heads: int,
     gen.manual_seed(seed)
     cpu_gen = torch.Generator()
     cpu_gen.manual_seed(seed + 7919)
-    src_dtype = "bf16" if kv_dtype == "fp8_e4m3" else kv_dtype
+    src_dtype = "bf16" if kv_dtype in FP8_MAX else kv_dtype
     if q_dtype is None:
         q_dtype = src_dtype
     B, Hq, Hkv, D, bs = len(seq_lens), num_q_heads, num_kv_heads, head_dim, block_size
@@ -226,7 +227,7 @@ def make_random(seq_lens: Sequence[int], *, num_q_heads: int, num_kv_heads: int,
     lens_old = [L - 1 for L in seq_lens]
     q = _randn(gen, (B, Hq, D), STORAGE[q_dtype], dev)
     hist = _fill_history(k_cache, v_cache, bt, lens_old, Hkv, D, bs, kv_dtype, gen, dev,
-                         src_dtype, write_direct=(kv_dtype != "fp8_e4m3"))
+                         src_dtype, write_direct=(kv_dtype not in FP8_MAX))
     new_key = _randn(gen, (B, Hkv, D), STORAGE[src_dtype], dev)
     new_value = _randn(gen, (B, Hkv, D), STORAGE[src_dtype], dev)
     slot_mapping = torch.cat([token_slots(bt, i, L - 1, L, bs) for i, L in enumerate(seq_lens)]) \
@@ -242,8 +243,8 @@ def make_random(seq_lens: Sequence[int], *, num_q_heads: int, num_kv_heads: int,
         wl.meta["needles"] = needles
     if hist is not None:
         wl.setup.append(("write", hist))
-    if kv_dtype == "fp8_e4m3":
-        wl.k_scale, wl.v_scale = _fp8_scales([hist], new_key, new_value)
+    if kv_dtype in FP8_MAX:
+        wl.k_scale, wl.v_scale = _fp8_scales([hist], new_key, new_value, kv_dtype)
     return wl
 
 
@@ -373,8 +374,8 @@ def prefix_share_fp16(seed: int = 3, prompt_len: int = 2048, num_prompts: int = 
 def long_ctx(kv_dtype: str = "bf16", seed: int = 4, lens: Sequence[int] = (32768,) * 4 + (131072,) * 4,
              needles: int = 0, gen_device="cpu") -> Workload:
     """Long context: 32 query / 8 KV heads, head_dim 128, block 32; lengths
-    {32768 x4, 131072 x4}; the pool holds exactly the blocks in use; bf16 or
-    fp8-e4m3 with per-tensor scales."""
+    {32768 x4, 131072 x4}; the pool holds exactly the blocks in use; bf16, or
+    fp8 (e4m3 or e5m2) with per-tensor scales."""
     return make_random(list(lens), num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=32,
                        kv_dtype=kv_dtype, q_dtype="bf16", seed=seed,
                        name=f"long_ctx_{kv_dtype}", needles=needles, gen_device=gen_device)

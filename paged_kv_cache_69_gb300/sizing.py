@@ -11,7 +11,7 @@ from __future__ import annotations
 
 from typing import Iterable
 
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1}
 
 
 def cdiv(a: int, b: int) -> int:

@@ -17,7 +17,8 @@ from paged_kv_cache_69_gb300 import inputs
 TOL = {"f32": dict(atol=1e-5, rtol=0.0, nrms=1e-5),
        "f16": dict(atol=2e-2, rtol=2e-2, nrms=1e-2),
        "bf16": dict(atol=2e-2, rtol=2e-2, nrms=1e-2),
-       "fp8_e4m3": dict(atol=6e-2, rtol=6e-2, nrms=3e-2)}
+       "fp8_e4m3": dict(atol=6e-2, rtol=6e-2, nrms=3e-2),
+       "fp8_e5m2": dict(atol=6e-2, rtol=6e-2, nrms=3e-2)}
 
 
 def oracle_caches(wl: inputs.Workload):

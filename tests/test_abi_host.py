@@ -53,7 +53,7 @@ def _decode_args(**over):
 @pytest.mark.parametrize("over,status", [
     (dict(Hq=5), pa.PA_OK + 1),                 # Hq not a multiple of Hkv -> invalid
     (dict(D=96), 2),                            # unsupported head_dim
-    (dict(bs=64), 2),                           # unsupported block size
+    (dict(bs=48), 2),                           # unsupported block size
     (dict(P=24), 1),                            # partition not a multiple of 16
     (dict(q=None), 1),                          # null pointer
     (dict(q=8), 1),                             # misaligned q
@@ -84,3 +84,24 @@ def test_cache_ops_host_validation(lib):
     # fp8 with a zero scale
     assert lib.pa_reshape_and_cache(16, 16, pa.PA_FP8_E4M3, 16, 16, f16, 16, 4, 2, 128, 16, 8, 0.0, 1.0, None, None) == 1
     assert lib.pa_copy_blocks(None, 16, f16, 16, 3, 2, 128, 16, 8, None, None) == 1
+
+
+def test_block_copy_host_validation(lib):
+    vp = ctypes.c_void_p
+    ptrs = (vp * 2)(16, 32)
+    # zero layers, too many layers, null pool pointer, unknown dtype
+    assert lib.pa_copy_blocks_layers(ptrs, ptrs, 0, pa.PA_F16, vp(16), 1, 2, 128, 16, 8, None, None) == 1
+    big = (vp * 257)(*([16] * 257))
+    assert lib.pa_copy_blocks_layers(big, big, 257, pa.PA_F16, vp(16), 1, 2, 128, 16, 8, None, None) == 2
+    nul = (vp * 2)(16, None)
+    assert lib.pa_copy_blocks_layers(nul, ptrs, 2, pa.PA_F16, vp(16), 1, 2, 128, 16, 8, None, None) == 1
+    assert lib.pa_copy_blocks_layers(ptrs, ptrs, 2, 9, vp(16), 1, 2, 128, 16, 8, None, None) == 1
+    # no pairs: nothing to do
+    assert lib.pa_copy_blocks_layers(ptrs, ptrs, 2, pa.PA_F16, None, 0, 2, 128, 16, 8, None, None) == 0
+    # swap: null pointers, misaligned pool, bad sizes
+    assert lib.pa_swap_blocks(None, vp(16), 8, vp(16), vp(16), 8, pa.PA_F16, vp(16), 1, 2, 128, 16,
+                              None, None) == 1
+    assert lib.pa_swap_blocks(vp(8), vp(16), 8, vp(16), vp(16), 8, pa.PA_F16, vp(16), 1, 2, 128, 16,
+                              None, None) == 1
+    assert lib.pa_swap_blocks(vp(16), vp(16), 0, vp(16), vp(16), 8, pa.PA_F16, vp(16), 1, 2, 128, 16,
+                              None, None) == 1

@@ -23,7 +23,8 @@ def _pool(NB, bs, Hkv, D, dtype):
 
 
 @pytest.mark.parametrize("kv,src", [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"),
-                                    ("fp8_e4m3", "f32"), ("fp8_e4m3", "f16"), ("fp8_e4m3", "bf16")])
+                                    ("fp8_e4m3", "f32"), ("fp8_e4m3", "f16"), ("fp8_e4m3", "bf16"),
+                                    ("fp8_e5m2", "f32"), ("fp8_e5m2", "f16"), ("fp8_e5m2", "bf16")])
 @pytest.mark.parametrize("Hkv,D,bs", [(2, 64, 16), (8, 128, 8), (4, 128, 32)])
 def test_reshape_and_cache_bit_exact(kv, src, Hkv, D, bs):
     NB, T = 64, 300
@@ -34,8 +35,9 @@ def test_reshape_and_cache_bit_exact(kv, src, Hkv, D, bs):
     slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
     slots[7] = -1
     slots[11] = NB * bs + 5
-    ks = float(key.float().nan_to_num(0, 0, 0).abs().max()) / 448.0 if kv == "fp8_e4m3" else 1.0
-    vs = float(val.float().abs().max()) / 448.0 if kv == "fp8_e4m3" else 1.0
+    fmax = inputs.FP8_MAX.get(kv)
+    ks = float(key.float().nan_to_num(0, 0, 0).abs().max()) / fmax if fmax else 1.0
+    vs = float(val.float().abs().max()) / fmax if fmax else 1.0
     k0, v0 = _pool(NB, bs, Hkv, D, kv), _pool(NB, bs, Hkv, D, kv)
     # oracle
     kr, vr = oracle.as_raw(k0).copy(), oracle.as_raw(v0).copy()
@@ -108,3 +110,59 @@ def test_fp8_quantiser_scaled_division():
                                 kv_dtype="fp8_e4m3", k_scale=scale, v_scale=scale)
         got = kc.view(-1).cpu().numpy()
         assert np.array_equal(got, oracle.encode_e4m3(x.numpy().reshape(-1), scale)), scale
+
+
+@pytest.mark.parametrize("kv", ["f16", "fp8_e4m3"])
+def test_copy_blocks_all_layers_bit_exact(kv):
+    NB, bs, Hkv, D, L = 48, 32, 2, 128, 5
+    g = torch.Generator().manual_seed(11)
+    dt = torch.uint8 if kv == "fp8_e4m3" else inputs.STORAGE[kv]
+    mk = lambda: (torch.randint(0, 255, (NB, bs, Hkv, D), generator=g, dtype=torch.uint8) if kv == "fp8_e4m3"
+                  else torch.randn(NB, bs, Hkv, D, generator=g).to(dt))
+    ks = [mk() for _ in range(L)]
+    vs = [mk() for _ in range(L)]
+    pairs = torch.tensor([[3, 40], [7, 41], [0, 47], [45, 1], [60, 2]], dtype=torch.int64)  # last: bad id
+    want_k = [oracle.as_raw(k).copy() for k in ks]
+    want_v = [oracle.as_raw(v).copy() for v in vs]
+    for wk, wv in zip(want_k, want_v):
+        assert oracle.copy_blocks(wk, wv, oracle.DTYPE_CODES[kv], oracle.as_raw(pairs), Hkv, D, bs, NB) == 1
+    kd, vd = [k.cuda() for k in ks], [v.cuda() for v in vs]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks_layers(kd, vd, pairs.cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == pa.ERRBIT_BAD_PAIR
+    for l in range(L):
+        assert np.array_equal(oracle.as_raw(kd[l]).view(np.uint8), want_k[l].view(np.uint8))
+        assert np.array_equal(oracle.as_raw(vd[l]).view(np.uint8), want_v[l].view(np.uint8))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_swap_out_and_in_through_pinned_host_memory(kv):
+    """A preempted request's blocks go to a pinned host pool and come back
+    into different device blocks; bit-exact against the oracle both ways."""
+    NB, NH, bs, Hkv, D = 64, 24, 16, 8, 128
+    g = torch.Generator().manual_seed(12)
+    dt = torch.uint8 if kv == "fp8_e4m3" else inputs.STORAGE[kv]
+    mk = lambda n: (torch.randint(0, 255, (n, bs, Hkv, D), generator=g, dtype=torch.uint8) if kv == "fp8_e4m3"
+                    else torch.randn(n, bs, Hkv, D, generator=g).to(dt))
+    dk, dv = mk(NB), mk(NB)
+    hk, hv = mk(NH).pin_memory(), mk(NH).pin_memory()
+    out_pairs = torch.tensor([[5, 0], [17, 1], [33, 2], [63, 3], [2, NH]], dtype=torch.int64)   # last: bad dst
+    want_hk, want_hv = oracle.as_raw(hk).copy(), oracle.as_raw(hv).copy()
+    assert oracle.swap_blocks(want_hk, want_hv, oracle.as_raw(dk), oracle.as_raw(dv), out_pairs.numpy()) == 1
+    dkc, dvc = dk.cuda(), dv.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_swap_blocks(hk, hv, dkc, dvc, out_pairs.cuda(), err_flag=err)         # swap out
+    torch.cuda.synchronize()
+    assert err.item() == pa.ERRBIT_BAD_PAIR
+    assert np.array_equal(oracle.as_raw(hk).view(np.uint8), want_hk.view(np.uint8))
+    assert np.array_equal(oracle.as_raw(hv).view(np.uint8), want_hv.view(np.uint8))
+    in_pairs = torch.tensor([[0, 40], [1, 41], [2, 42], [3, 43]], dtype=torch.int64)
+    want_dk, want_dv = oracle.as_raw(dk).copy(), oracle.as_raw(dv).copy()
+    assert oracle.swap_blocks(want_dk, want_dv, oracle.as_raw(hk), oracle.as_raw(hv), in_pairs.numpy()) == 0
+    err.zero_()
+    pa.pa_swap_blocks(dkc, dvc, hk, hv, in_pairs.cuda(), err_flag=err)           # swap in
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(oracle.as_raw(dkc).view(np.uint8), want_dk.view(np.uint8))
+    assert np.array_equal(oracle.as_raw(dvc).view(np.uint8), want_dv.view(np.uint8))

@@ -52,6 +52,11 @@ CASES = [
     ("fp8_e4m3", "bf16", 128, 8, 16, 4, [1, 8, 9, 31, 32, 33, 300]),   # four 8-row boxes per 32-token chunk
     ("fp8_e4m3", "bf16", 128, 16, 8, 8, [2, 47, 64, 65]),             # G = 1
     ("fp8_e4m3", "f16", 128, 16, 32, 2, [7, 100, 513]),               # G = 16: e4m3 -> f16 kernel
+    ("fp8_e5m2", "bf16", 128, 16, 32, 8, [1, 31, 32, 33, 900]),       # e5m2: byte-permute widening
+    ("fp8_e5m2", "f16", 128, 32, 28, 4, [5, 64, 65, 400]),
+    ("bf16", None, 128, 64, 32, 8, [1, 63, 64, 65, 700]),      # large blocks: several chunks per block
+    ("f16", None, 128, 128, 28, 4, [5, 127, 128, 129, 1500]),
+    ("fp8_e4m3", "bf16", 128, 128, 32, 8, [31, 128, 129, 1000]),
     ("f32", None, 128, 16, 8, 2, [3, 17, 90]),
     ("f32", None, 64, 8, 6, 3, [1, 8, 9, 64]),
 ]
@@ -280,7 +285,7 @@ def test_full_prefix_sharing_fp16(prompt_len):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "fp8_e5m2"])
 def test_full_long_context(kv):
     _sampled_check(inputs.long_ctx(kv, gen_device="cuda"), samples=12)
 
