@@ -17,6 +17,9 @@ Parity status of each function (what pins it, see tests/test_oracle_*.py):
     invariants, brute force on tiny cases, and planted-mistake checks.
   - reshape_and_cache / copy_blocks: numpy fancy-indexing restatements and
     the copy-on-write worked example of "vLLM intro part 2", section 5.
+  - attention_causal (several query tokens per request): one token equals
+    decode, dense causal attention in numpy on a contiguous layout, keys
+    after a token's position do not change it, the last token equals decode.
 """
 import ctypes
 import os
@@ -161,6 +164,38 @@ def decode(p: Problem) -> np.ndarray:
     rc = lib().pao_decode(_ptr(out), *p._common())
     if rc != 0:
         raise ValueError(f"oracle decode failed with status {rc}")
+    return out
+
+
+def attention_causal(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, q_start,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     k_scale=1.0, v_scale=1.0) -> np.ndarray:
+    """Several new tokens of a request attended in one step (chunked prefill
+    or speculative lookahead: the "new" and "lookahead" spans of one
+    request in one iteration, "分页省的不是 KV 字节" section 2, the
+    allocate_slots layout), their K/V already in the pool.  Sequence i has
+    n_i = q_start[i+1] - q_start[i] query rows (rows q_start[i] .. of q,
+    [total, Hq, D]), the last n_i of its L_i = seq_lens[i] tokens; query
+    token j sits at position p = L_i - n_i + j and attends keys 0..p (causal).
+    Written as the definition: the decode of that one token over the prefix of
+    length p + 1.  Returns float64 [total, Hq, D]."""
+    qr = as_raw(q)
+    kr, vr = as_raw(k_cache), as_raw(v_cache)
+    bt = np.ascontiguousarray(as_raw(block_tables), dtype=np.int32)
+    sl = np.asarray(as_raw(seq_lens), dtype=np.int64)
+    qs = np.asarray(as_raw(q_start), dtype=np.int64)
+    out = np.zeros((qr.shape[0], num_q_heads, head_dim), dtype=np.float64)
+    for i in range(sl.shape[0]):
+        n = int(qs[i + 1] - qs[i])
+        for j in range(n):
+            pos = int(sl[i]) - n + j
+            if pos < 0:
+                continue                                  # no such position: zeros
+            row = int(qs[i]) + j
+            prob = Problem(qr[row:row + 1], q_dtype, kr, vr, kv_dtype, bt[i:i + 1],
+                           np.array([pos + 1], np.int32), num_q_heads, num_kv_heads, head_dim,
+                           block_size, num_blocks, scale, k_scale, v_scale)
+            out[row] = decode(prob)[0]
     return out
 
 
