@@ -265,6 +265,16 @@ def run_ours(args, rank, world, local) -> dict | None:
     MB = d.block_tables.shape[1]
     ws = pa.alloc_workspace(d.num_seqs, d.num_q_heads, d.head_dim, MB * d.block_size, args.partition_tokens,
                             device=device)
+    NQ = max(1, args.q_per_seq)
+    if NQ > 1:
+        # speculative-decoding step: the last NQ tokens of every sequence are queries (causal)
+        gq = torch.Generator(device=device)
+        gq.manual_seed(17)
+        q_mq = torch.randn(d.num_seqs * NQ, d.num_q_heads, d.head_dim, generator=gq, device=device).to(d.q.dtype)
+        out_mq = torch.empty_like(q_mq)
+        qs_mq = torch.arange(0, d.num_seqs * NQ + 1, NQ, dtype=torch.int32, device=device)
+        ws = torch.empty(pa.pa_attention_workspace_size(d.num_seqs, NQ, d.num_q_heads, d.head_dim, MB * d.block_size,
+                                                        args.partition_tokens), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
     pairs = d.cow_pairs if (d.cow_pairs is not None and d.cow_pairs.numel()) else None
 
@@ -273,6 +283,10 @@ def run_ours(args, rank, world, local) -> dict | None:
                                 v_scale=d.v_scale, err_flag=err)
 
     def decode(q_, bt_, sl_, out_):
+        if NQ > 1:
+            pa.pa_attention(out_mq, q_mq, d.k_cache, d.v_cache, bt_, sl_, qs_mq, d.scale, NQ, k_scale=d.k_scale,
+                            v_scale=d.v_scale, partition_tokens=args.partition_tokens, workspace=ws, err_flag=err)
+            return
         pa.pa_decode(out_, q_, d.k_cache, d.v_cache, bt_, sl_, d.scale, k_scale=d.k_scale, v_scale=d.v_scale,
                      partition_tokens=args.partition_tokens, workspace=ws, err_flag=err, simt=args.simt)
 
@@ -317,7 +331,7 @@ def run_ours(args, rank, world, local) -> dict | None:
 
     # ---- end to end: host buffers, copies inside the timed region ----
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and NQ == 1:
         host = [x.cpu().pin_memory() for x in (d.q, d.new_key, d.new_value, d.slot_mapping, d.block_tables,
                                                 d.seq_lens)]
         stage = [torch.empty_like(x) for x in (d.q, d.new_key, d.new_value, d.slot_mapping, d.block_tables,
@@ -354,25 +368,30 @@ def run_ours(args, rank, world, local) -> dict | None:
     lens = wl.seq_lens.tolist()
     alg = sizing.decode_algorithmic_bytes(lens, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
                                           wl.q_dtype)
+    # queries and outputs of the extra query tokens
+    alg += (NQ - 1) * wl.num_seqs * wl.num_q_heads * wl.head_dim * 2 * sizing.ELEM_BYTES[wl.q_dtype]
     if wl.meta.get("unique_tokens"):
         # shared prefix blocks are read once from HBM: count each unique token once
         alg = (wl.meta["unique_tokens"] * wl.num_kv_heads * wl.head_dim * sizing.ELEM_BYTES[wl.kv_dtype] * 2 +
                wl.num_seqs * wl.num_q_heads * wl.head_dim * 2 * sizing.ELEM_BYTES[wl.q_dtype])
     peak, peak_src = measured_peak()
     achieved = alg / (dec_ms / 1e3) / 1e9
-    value = wl.num_seqs * world * K / (ms_total / 1e3)
+    value = wl.num_seqs * NQ * world * K / (ms_total / 1e3)
     res = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
            "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": wl.kv_dtype, "data": "synthetic",
            "config": workload_config(wl, {"l2": "inputs larger than L2 (K+V pool streamed each step)",
                                           "decode_variant": "cuda-core" if args.simt else "tensor-core",
                                           "partition_tokens": args.partition_tokens,
+                                          "query_tokens_per_seq": NQ,
                                           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
            "kv_gbs": achieved, "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                         "frac": achieved / peak, "peak_source": peak_src,
-                        "kernel": "pa_decode (main + reduce)", "algorithmic_bytes_per_launch": alg,
-                        "launch_ms": dec_ms, "traffic": profile_traffic(args.workload)},
+                        "kernel": "pa_decode (main + reduce)" if NQ == 1 else "pa_attention (main + reduce)",
+                        "algorithmic_bytes_per_launch": alg,
+                        "launch_ms": dec_ms,
+                        "traffic": profile_traffic(args.workload) if NQ == 1 and not args.partition_tokens else None},
            "gpu_launches": K * (3 + (1 if pairs is not None else 0)),
            "clocks": clk, "e2e": e2e}
     if not args.no_cpu_baseline and world == 1:
@@ -445,6 +464,69 @@ def run_block_manager(args) -> dict:
                              "sample": f"first {o_n} requests, 5 steps, scaled to {n} requests"}}
 
 
+# ---------------------------------------------------------------------------
+# block copies: all-layer copy-on-write and swap through pinned host memory
+# ---------------------------------------------------------------------------
+def run_block_copy(args) -> dict:
+    import torch
+    import paged_kv_cache_69_gb300 as pa
+    torch.cuda.set_device(0)
+    dev = "cuda"
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e-3          # seconds per call
+
+    # swap: 4096 scattered blocks of the 7B-like layer (16 x 4 x 128 fp16 = 16 KB each for K and V)
+    NB, NH, bs, Hkv, D, P = 40000, 4096, 16, 4, 128, 4096
+    g = torch.Generator().manual_seed(0)
+    dk = torch.randn(NB, bs, Hkv, D, device=dev, dtype=torch.float16)
+    dv = torch.randn(NB, bs, Hkv, D, device=dev, dtype=torch.float16)
+    hk = torch.empty(NH, bs, Hkv, D, dtype=torch.float16).pin_memory()
+    hv = torch.empty(NH, bs, Hkv, D, dtype=torch.float16).pin_memory()
+    src = torch.randperm(NB, generator=g)[:P]
+    out_pairs = torch.stack([src, torch.arange(P)], 1).to(dev)
+    in_pairs = torch.stack([torch.arange(P), torch.randperm(NB, generator=g)[:P]], 1).to(dev)
+    block_bytes = bs * Hkv * D * 2
+    moved = 2 * P * block_bytes                                   # K and V
+    t_out = timed(lambda: pa.pa_swap_blocks(hk, hv, dk, dv, out_pairs), 20)
+    t_in = timed(lambda: pa.pa_swap_blocks(dk, dv, hk, hv, in_pairs), 20)
+    flat_d = torch.empty(moved // 2, dtype=torch.float16, device=dev)
+    flat_h = torch.empty(moved // 2, dtype=torch.float16).pin_memory()
+    t_flat_out = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), 20)
+    t_flat_in = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), 20)
+    # all-layer copy-on-write: 96 pairs (the prefix-sharing COW step) in 28 layers
+    L, NB2, pairs_n = 28, 4096, 96
+    ks = [torch.randn(NB2, bs, Hkv, D, device=dev, dtype=torch.float16) for _ in range(L)]
+    vs = [torch.randn(NB2, bs, Hkv, D, device=dev, dtype=torch.float16) for _ in range(L)]
+    perm = torch.randperm(NB2, generator=g)
+    cow = torch.stack([perm[:pairs_n], perm[pairs_n:2 * pairs_n]], 1).to(dev)
+    t_cow = timed(lambda: pa.pa_copy_blocks_layers(ks, vs, cow), 50)
+    cow_bytes = L * pairs_n * 2 * block_bytes * 2                 # K and V, read + write
+    peak, src_peak = measured_peak()
+    return {"metric": "block copies: swap through pinned host memory and all-layer copy-on-write",
+            "component": "block_copy", "unit": "GB/s", "higher_is_better": True,
+            "value": moved / t_out / 1e9,
+            "config": {"workload": "4096 scattered 32 KB blocks (K+V, 7B-like layer) out to pinned host and back; "
+                                   "96 COW pairs x 28 layers", "block_bytes_k_or_v": block_bytes},
+            "swap_out_gbs": moved / t_out / 1e9, "swap_in_gbs": moved / t_in / 1e9,
+            "contiguous_d2h_gbs": moved / t_flat_out / 1e9, "contiguous_h2d_gbs": moved / t_flat_in / 1e9,
+            "swap_out_frac_of_contiguous": t_flat_out / t_out, "swap_in_frac_of_contiguous": t_flat_in / t_in,
+            "cow_all_layers_us": t_cow * 1e6, "cow_all_layers_gbs": cow_bytes / t_cow / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "block_copy_kernel (28-layer COW)",
+                         "achieved": cow_bytes / t_cow / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": cow_bytes / t_cow / 1e9 / peak, "peak_source": src_peak, "traffic": None}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,15 +536,18 @@ def main():
     ap.add_argument("--workload", default="qwen7b_fp16")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--simt", action="store_true", help="time the CUDA-core decode variant")
+    ap.add_argument("--q-per-seq", type=int, default=1,
+                    help="query tokens per sequence (>1: speculative-decoding step through pa_attention)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--component", choices=["decode", "block_manager"], default="decode",
-                    help="block_manager: time the host allocator instead of the GPU path")
+    ap.add_argument("--component", choices=["decode", "block_manager", "block_copy"], default="decode",
+                    help="block_manager: the host allocator; block_copy: swap and all-layer copies")
     args = ap.parse_args()
-    if args.component == "block_manager":
+    if args.component != "decode":
         if int(os.environ.get("RANK", "0")) == 0:
-            print(json.dumps(run_block_manager(args)))
+            run = run_block_manager if args.component == "block_manager" else run_block_copy
+            print(json.dumps(run(args)))
         return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -6,7 +6,8 @@
  *   pa_copy_blocks        copy-on-write of shared blocks (one layer, or
  *                         all layers: pa_copy_blocks_layers),
  *   pa_swap_blocks        block copies between a device and a host pool,
- *   pa_decode             one decode step of attention over a paged pool.
+ *   pa_decode             one decode step of attention over a paged pool,
+ *   pa_attention          several causal query tokens per sequence.
  *
  * Layouts (row-major, innermost last):
  *   k_cache, v_cache   [num_blocks, block_size, num_kv_heads, head_dim]
@@ -212,6 +213,35 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype kv_dtype,
                          const int64_t* block_mapping, int num_pairs,
                          int num_kv_heads, int head_dim, int block_size,
                          int num_blocks, int32_t* err_flag, cudaStream_t stream);
+
+/*
+ * pa_attention -- causal attention of several new query tokens per sequence
+ * over the paged pool, their K/V already written (speculative lookahead
+ * tokens, or a chunk of a prompt: the "new" and "lookahead" spans one request
+ * computes in one iteration, "分页省的不是 KV 字节", section 2, the
+ * allocate_slots layout).  Sequence i owns query rows q_start[i] ..
+ * q_start[i+1]-1 of q and out ([total_q, num_q_heads, head_dim]); they are the
+ * last n_i = q_start[i+1] - q_start[i] of its L_i = seq_lens[i] tokens, and
+ * query token j, at position p = L_i - n_i + j, attends keys 0..p:
+ *   out[q_start[i] + j, h] = sum_{t<=p} softmax_t(scale * <q, K_t>) V_t.
+ * A token with p < 0 (n_i > L_i) gets zeros.  One pass reads each K/V byte
+ * once for all of a sequence's query tokens: the (token, head) rows of a GQA
+ * group share the MMA tile.  q_start is a device int32 array of num_seqs + 1
+ * entries, non-decreasing, q_start[0] = 0, q_start[num_seqs] = total_q; every
+ * n_i <= max_q_len, and max_q_len * (num_q_heads / num_kv_heads) <= 128.
+ * Tensor cores only (f16, bf16 and fp8 caches); other arguments as for
+ * pa_decode.  With every n_i = 1 the result equals pa_decode's.
+ */
+size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int head_dim,
+                                   int max_seq_len, int partition_tokens);
+pa_status pa_attention(void* out, const void* q, pa_dtype q_dtype,
+                       const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens, const int32_t* q_start, int num_seqs,
+                       int total_q, int max_q_len, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, int num_blocks, float scale,
+                       float k_scale, float v_scale, int partition_tokens, void* workspace,
+                       size_t workspace_bytes, int32_t* err_flag, cudaStream_t stream);
 
 /*
  * pa_copy_blocks_layers -- pa_copy_blocks for every layer of a model in one

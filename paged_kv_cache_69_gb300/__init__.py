@@ -25,7 +25,7 @@ ERRBIT_BAD_BLOCK, ERRBIT_BAD_SLOT, ERRBIT_BAD_PAIR, ERRBIT_SEQ_TOO_LONG, ERRBIT_
 # entry points declared in include/pa.h
 EXPORTED = ("pa_status_string", "pa_last_error_detail", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_simt", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks",
-            "pa_copy_blocks_layers", "pa_swap_blocks")
+            "pa_copy_blocks_layers", "pa_swap_blocks", "pa_attention", "pa_attention_workspace_size")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _DTYPE_CODE = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16,
@@ -72,6 +72,11 @@ def _configure(L):
     L.pa_copy_blocks_layers.argtypes = [vp, vp, c_int, c_int, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]
     L.pa_swap_blocks.restype = c_int
     L.pa_swap_blocks.argtypes = [vp, vp, c_int, vp, vp, c_int, c_int, vp, c_int, c_int, c_int, c_int, vp, vp]
+    L.pa_attention_workspace_size.restype = sz
+    L.pa_attention_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int]
+    L.pa_attention.restype = c_int
+    L.pa_attention.argtypes = [vp, vp, c_int, vp, vp, c_int, vp, c_int, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                               c_int, c_int, c_int, c_float, c_float, c_float, c_int, vp, sz, vp, vp]
     return L
 
 
@@ -254,3 +259,42 @@ def pa_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor
     _check(lib().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), NBd, _ptr(src_k), _ptr(src_v), NBs,
                                 _code(dst_k, kv_dtype), _ptr(block_mapping), block_mapping.numel() // 2,
                                 Hkv, D, bs, _ptr(err_flag), _stream(stream)))
+
+
+def pa_attention_workspace_size(num_seqs: int, max_q_len: int, num_q_heads: int, head_dim: int,
+                                max_seq_len: int, partition_tokens: int = 0) -> int:
+    return int(lib().pa_attention_workspace_size(num_seqs, max_q_len, num_q_heads, head_dim, max_seq_len,
+                                                 partition_tokens))
+
+
+def pa_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, seq_lens: torch.Tensor, q_start: torch.Tensor, scale: float,
+                 max_q_len: int, kv_dtype=None, *, k_scale: float = 1.0, v_scale: float = 1.0,
+                 partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                 err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of several query tokens per sequence over the paged
+    pool.  q/out [T, Hq, D]; sequence i's query rows are q_start[i] ..
+    q_start[i+1]-1 (int32 [B+1] on the device), the last tokens of its
+    seq_lens[i]; max_q_len bounds every sequence's query count."""
+    _dev(out, q, k_cache, v_cache, block_tables, seq_lens, q_start, workspace, err_flag)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    B = seq_lens.shape[0]
+    if D2 != D or tuple(out.shape) != (T, Hq, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out, k_cache and v_cache")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32 or q_start.dtype != torch.int32:
+        raise ValueError("block_tables, seq_lens and q_start must be int32")
+    if q_start.numel() != B + 1:
+        raise ValueError("q_start must have num_seqs + 1 entries")
+    MB = block_tables.shape[1]
+    if workspace is None:
+        n = pa_attention_workspace_size(B, max_q_len, Hq, D, MB * bs, partition_tokens)
+        if n == 0:
+            raise PaError(1, "invalid workspace bounds")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(lib().pa_attention(_ptr(out), _ptr(q), _code(q), _ptr(k_cache), _ptr(v_cache), _code(k_cache, kv_dtype),
+                              _ptr(block_tables), MB, _ptr(seq_lens), _ptr(q_start), B, T, int(max_q_len), Hq, Hkv,
+                              D, bs, NB, float(scale), float(k_scale), float(v_scale), int(partition_tokens),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_flag),
+                              _stream(stream)))
+    return out

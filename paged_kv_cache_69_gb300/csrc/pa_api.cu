@@ -124,6 +124,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int cdiv_h(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+// Hq here counts partial rows per slot: query heads x query tokens per sequence.
 static size_t workspace_bytes_for(int B, int Hq, int D, int max_seq_len, int partition_tokens, int sms) {
     const long long nr_cap = 2LL * sms;
     const long long units = partition_tokens > 0 ? static_cast<long long>(B) * cdiv_h(max_seq_len, partition_tokens)
@@ -140,11 +141,15 @@ static int max_slots_for(int B, int max_seq_len, int partition_tokens, int sms) 
     return static_cast<int>(std::min<long long>(2LL * sms + units, 0x7fffffffLL));
 }
 
+// q_start == nullptr: one query per sequence (decode); otherwise sequence i
+// has q_start[i+1] - q_start[i] <= QL query rows starting at row q_start[i].
 static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
                              const void* v_cache, pa_dtype kv_dtype, const int32_t* block_tables, int MB,
                              const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int bs, int NB,
                              float scale, float k_scale, float v_scale, int partition_tokens,
-                             void* workspace, size_t workspace_bytes, int32_t* err_flag, cudaStream_t stream) {
+                             void* workspace, size_t workspace_bytes, int32_t* err_flag, cudaStream_t stream,
+                             const int32_t* q_start = nullptr, int QL = 1, int total_q = 0) {
+    const bool mq = q_start != nullptr;
     clear_error();
     if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || bs <= 0 || NB <= 0 || MB <= 0)
         return fail(PA_ERR_INVALID_ARG, "decode: sizes must be positive (num_seqs >= 0)");
@@ -173,13 +178,17 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     }
     if (tc && kv_dtype == PA_F32)
         return fail(PA_ERR_UNSUPPORTED, "decode: f32 caches run on the CUDA-core path (pa_decode_simt)");
+    if (mq && (!tc || QL < 1 || total_q < 0 || static_cast<long long>(QL) * (Hq / Hkv) > 128))
+        return fail(PA_ERR_UNSUPPORTED,
+                    "attention: several query tokens need the tensor-core path and max_q_len * G <= 128");
     // fp8 caches on the tensor-core path run the native-e4m3 kernel (32-token
     // chunks, GQA groups of up to 8 heads, partitions a multiple of 32
     // tokens); other fp8 shapes convert e4m3 to f16 in registers.
-    const bool native8 = tc && kv_dtype == PA_FP8_E4M3 && D == 128 && Hq / Hkv <= 8 &&
+    const bool native8 = !mq && tc && kv_dtype == PA_FP8_E4M3 && D == 128 && Hq / Hkv <= 8 &&
                          partition_tokens % 32 == 0;
     const int CT = native8 ? 32 : 16;
-    const void* kern = native8 ? decode_kernel_e4m3(q_dtype, D)
+    const void* kern = mq      ? decode_kernel_mq(kv_dtype, q_dtype, D)
+                       : native8 ? decode_kernel_e4m3(q_dtype, D)
                        : tc    ? decode_kernel_tc(kv_dtype, q_dtype, D)
                                : decode_kernel_simt(kv_dtype, q_dtype, D);
     if (!kern) return fail(PA_ERR_UNSUPPORTED, "decode: no kernel for this dtype / head_dim combination");
@@ -192,12 +201,15 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     const int G = Hq / Hkv;
     const int e = dtype_bytes(kv_dtype);
     const int eq = dtype_bytes(q_dtype);
-    const int MT = cdiv_h(G, 16);
-    if (MT > 8) return fail(PA_ERR_UNSUPPORTED, "decode: more than 128 query heads per KV head");
+    const int MT = cdiv_h(static_cast<long long>(QL) * G, 16);   // 16-row tiles of (query token, head) rows
+    if (MT > 8) return fail(PA_ERR_UNSUPPORTED, "decode: more than 128 query rows per KV head");
     int HPC = 0;
+    // several query tokens: at most 4 consumer warps per CTA when the rows
+    // take more than one tile, so that two CTAs share an SM
+    const int max_warps = (mq && MT > 1) ? 4 : 8;
     for (int h = Hkv; h >= 1; --h) {
         if (Hkv % h) continue;
-        if (h * MT > 8) continue;
+        if (h * MT > std::max(max_warps, MT)) continue;
         if (static_cast<long long>(CT) * h * D * e > 32 * 1024) continue;
         HPC = h;
         break;
@@ -216,6 +228,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.HPC = HPC; p.NHG = NHG; p.MT = MT; p.NCW = NCW;
     p.ct = CT;
     p.PC = partition_tokens / CT;
+    p.q_start = q_start;
+    p.QL = QL;
     // Schedule weights: a unit start (query rows loaded, result written)
     // is charged 3/4 of a chunk, which balanced CTA finish times best on
     // length mixes with many short sequences.
@@ -224,7 +238,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.rpb = rpb;
     p.box_bytes = static_cast<uint32_t>(rpb * HPC * DH * 128);
     p.kv_bytes = static_cast<uint32_t>(CT * HPC * D * e);
-    p.q_bytes = static_cast<uint32_t>(HPC * G * D * eq);
+    p.q_bytes = static_cast<uint32_t>(QL * HPC * G * D * eq);
     p.q_slot_bytes = (p.q_bytes + 1023u) & ~1023u;   // swizzled tensor copies need 1024-B alignment
     p.stage_bytes = 2 * p.kv_bytes;
     const uint32_t simtq = tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
@@ -244,7 +258,9 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     if (by_regs >= 2) {
         const long long per_cta = sm_smem / 2 - 1024 - fixed;
         const int s2 = static_cast<int>(std::min<long long>(MAX_STAGES, per_cta / p.stage_bytes));
-        if (s2 >= 3) stages = s2;
+        // the multi-token query ring takes more shared memory: two stages
+        // per CTA still keep four in flight per SM
+        if (s2 >= (mq ? 2 : 3)) stages = s2;
     }
     if (stages == 0) {
         const long long per_cta = std::min(dev.max_smem, 227 * 1024) - static_cast<long long>(fixed);
@@ -264,7 +280,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.v_scale = is_fp8(kv_dtype) ? v_scale : 1.f;
 
     // workspace
-    const size_t need = workspace_bytes_for(B, Hq, D, MB * bs, partition_tokens, dev.sms);
+    const int prow = QL * Hq;                         // partial rows per slot
+    const size_t need = workspace_bytes_for(B, prow, D, MB * bs, partition_tokens, dev.sms);
     if (!workspace) return fail(PA_ERR_WORKSPACE, "decode: workspace pointer is null");
     if (workspace_bytes < need) return fail(PA_ERR_WORKSPACE, "decode: workspace smaller than pa_decode_workspace_size()");
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PA_ERR_WORKSPACE, "decode: workspace must be 256-byte aligned");
@@ -272,7 +289,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.split_list = reinterpret_cast<int4*>(ws); ws += align256(sizeof(int4) * static_cast<size_t>(B));
     p.totals = reinterpret_cast<int*>(ws); ws += 256;
     p.max_slots = max_slots_for(B, MB * bs, partition_tokens, dev.sms);
-    p.part_ml = reinterpret_cast<float2*>(ws); ws += align256(sizeof(float2) * static_cast<size_t>(p.max_slots) * Hq);
+    p.part_ml = reinterpret_cast<float2*>(ws); ws += align256(sizeof(float2) * static_cast<size_t>(p.max_slots) * prow);
     p.part_acc = reinterpret_cast<float*>(ws);
 
     // tensor maps
@@ -296,7 +313,22 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     alignas(64) CUtensorMap tq;
     std::memset(&tq, 0, sizeof tq);
     p.q_tma = 0;
-    if (tc) {
+    if (mq) {
+        // [column block][token][head][128 B]: QL tokens x HPC*G heads per copy
+        const EncodeTiledFn enc = encode_fn();
+        const cuuint32_t e128q = static_cast<cuuint32_t>(128 / eq);
+        const cuuint32_t dhq = static_cast<cuuint32_t>(D * eq / 128);
+        cuuint64_t dims[4] = {e128q, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(std::max(total_q, 1)), dhq};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * eq, static_cast<cuuint64_t>(Hq) * D * eq, 128};
+        cuuint32_t box[4] = {e128q, static_cast<cuuint32_t>(HPC * G), static_cast<cuuint32_t>(QL), dhq};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (!enc || HPC * G > 256 || QL > 256 ||
+            enc(&tq, tmap_type(q_dtype), 4, const_cast<void*>(q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(PA_ERR_CUDA, "attention: query tensor map could not be encoded");
+        p.q_tma = 1;
+    } else if (tc) {
         const EncodeTiledFn enc = encode_fn();
         const cuuint32_t e128q = static_cast<cuuint32_t>(128 / eq);
         const cuuint32_t dhq = static_cast<cuuint32_t>(D * eq / 128);
@@ -343,8 +375,9 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         int red_per_sm = 0;
         ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&red_per_sm, rkern, RED_THREADS, 0);
         if (ce != cudaSuccess) return fail_cuda("decode: reduce occupancy query", ce);
-        const long long items = split_heads ? static_cast<long long>(B) * Hq
-                                            : static_cast<long long>(B) * ((Hq + RED_THREADS / 32 - 1) / (RED_THREADS / 32));
+        const long long items = static_cast<long long>(QL) *
+                                (split_heads ? static_cast<long long>(B) * Hq
+                                             : static_cast<long long>(B) * ((Hq + RED_THREADS / 32 - 1) / (RED_THREADS / 32)));
         const long long g = std::max(1LL, std::min(items, static_cast<long long>(std::max(1, red_per_sm)) * dev.sms));
         rcfg.gridDim = dim3(static_cast<unsigned>(g));
     }
@@ -407,4 +440,31 @@ extern "C" pa_status pa_decode_simt(void* out, const void* q, pa_dtype q_dtype, 
     return decode_impl(false, out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, max_blocks_per_seq,
                        seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                        k_scale, v_scale, partition_tokens, workspace, workspace_bytes, err_flag, stream);
+}
+
+extern "C" size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int head_dim,
+                                              int max_seq_len, int partition_tokens) {
+    if (num_seqs < 0 || max_q_len <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
+        partition_tokens < 0)
+        return 0;
+    DeviceInfo dev;
+    if (!device_info(dev)) return 0;
+    return workspace_bytes_for(num_seqs, max_q_len * num_q_heads, head_dim, max_seq_len, partition_tokens, dev.sms);
+}
+
+extern "C" pa_status pa_attention(void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
+                                  const void* v_cache, pa_dtype kv_dtype, const int32_t* block_tables,
+                                  int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_start,
+                                  int num_seqs, int total_q, int max_q_len, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int num_blocks, float scale, float k_scale,
+                                  float v_scale, int partition_tokens, void* workspace, size_t workspace_bytes,
+                                  int32_t* err_flag, cudaStream_t stream) {
+    clear_error();
+    if (!q_start) return fail(PA_ERR_INVALID_ARG, "attention: q_start is null");
+    if (max_q_len < 1 || total_q < 0) return fail(PA_ERR_INVALID_ARG, "attention: max_q_len must be >= 1");
+    if (num_seqs > 0 && total_q == 0) return PA_OK;
+    return decode_impl(true, out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, max_blocks_per_seq,
+                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                       k_scale, v_scale, partition_tokens, workspace, workspace_bytes, err_flag, stream,
+                       q_start, max_q_len, total_q);
 }

@@ -132,7 +132,23 @@ block_copy_kernel(const __grid_constant__ BlockCopyArgs a) {
     const uint4* s = reinterpret_cast<const uint4*>(a.src[kv][l] + src * a.block_bytes);
     uint4* d = reinterpret_cast<uint4*>(a.dst[kv][l] + dst * a.block_bytes);
     const int64_t n = a.block_bytes / 16;
-    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) d[k] = s[k];
+    // Up to U vectors per thread are loaded before any is stored: the
+    // compiler cannot prove source and destination blocks apart, and would
+    // otherwise wait for each load before the next.
+    constexpr int U = 8;
+    for (int64_t k0 = threadIdx.x; k0 < n; k0 += static_cast<int64_t>(U) * blockDim.x) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = k0 + static_cast<int64_t>(u) * blockDim.x;
+            if (k < n) r[u] = s[k];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = k0 + static_cast<int64_t>(u) * blockDim.x;
+            if (k < n) d[k] = r[u];
+        }
+    }
 }
 
 // Validates and launches a block copy over num_layers pools.

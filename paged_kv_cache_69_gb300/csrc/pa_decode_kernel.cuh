@@ -51,10 +51,12 @@ struct StageDesc {
     int tok0;
     int slot;
     uint32_t vmask;
-    uint32_t flags;
+    uint32_t flags;          // SEG_* bits; bits 16.. hold the sequence's query count
     int qslot;               // query ring slot holding this segment's rows
-    int pad[2];
+    int qrow0;               // row of the sequence's first query token in q / out
+    int qpos0;               // its position in the sequence (queries are the last tokens)
 };
+constexpr int QCOUNT_SHIFT = 16;
 
 struct DecodeParams {
     void* out;
@@ -72,6 +74,8 @@ struct DecodeParams {
     int HPC, NHG, NR, MT, NCW;
     int ct;                   // tokens per chunk (pipeline stage): 16, or 32 for native e4m3
     int PC;                   // partition length in chunks, 0 = none
+    const int32_t* q_start;   // several query tokens per sequence: [B+1] row offsets; null = one each
+    int QL;                   // most query tokens of a sequence (1 for decode)
     int WQ, WS;               // schedule weights of a chunk and of a unit start
     int max_slots;
     float qk_scale;           // scale * log2(e) (* k_scale for fp8)
@@ -323,7 +327,7 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16*
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v[0], v[1], true), pack2(v[2], v[3], true));
 }
 
-template <class KV, class QT, int D, bool TC, int CT>
+template <class KV, class QT, int D, bool TC, int CT, bool MQ = false>
 struct DecodeKernel {
     using KT = typename KV::T;
     using QE = typename QT::T;
@@ -369,6 +373,19 @@ struct DecodeKernel {
         load_lens(pl.seq);
         int i = pl.seq, Si = pl.S, Ui = pl.U;
         int L = len_of(i);
+        // first query row and query count of sequence i (one per sequence in decode)
+        int qrow_i = i, qn_i = 1;
+        auto load_q_rows = [&]() {
+            if constexpr (MQ) {
+                const int a = i < p.B ? __ldg(p.q_start + i) : 0;
+                const int b = i < p.B ? __ldg(p.q_start + i + 1) : 0;
+                qrow_i = a;
+                qn_i = b - a;
+            } else {
+                qrow_i = i;
+            }
+        };
+        load_q_rows();
         int nch = cdiv_i(L, CT), nbl = cdiv_i(L, p.bs);
         int j = pl.cs - Si;
         const int nb = p.bs >= CT ? 1 : CT / p.bs;      // boxes per chunk
@@ -390,6 +407,7 @@ struct DecodeKernel {
             while (j >= nch) {
                 Si += nch; Ui += n_units(L, p.PC, p.ct); ++i;
                 L = len_of(i);
+                load_q_rows();
                 nch = cdiv_i(L, CT); nbl = cdiv_i(L, p.bs); j = 0;
                 wbase = 0;
                 wval = (nseq == i && nbase == 0) ? nval : load_win(i, 0, nbl);
@@ -455,9 +473,12 @@ struct DecodeKernel {
                     const int nu = n_units(L, p.PC, p.ct);
                     if (nu == 1 && Si >= pl.cs && Si + nch <= pl.ce) flags |= DIRECT;
                     StageDesc d;
-                    d.seq = i; d.tok0 = tok0; d.vmask = vmask; d.flags = flags;
+                    d.seq = i; d.tok0 = tok0; d.vmask = vmask;
+                    d.flags = flags | (static_cast<uint32_t>(qn_i) << QCOUNT_SHIFT);
                     d.slot = (blockIdx.x / p.NHG) + Ui + (p.PC > 0 ? j / p.PC : 0);
                     d.qslot = qs;
+                    d.qrow0 = qrow_i;
+                    d.qpos0 = L - qn_i;
                     descs[slot] = d;
                     const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (seg_start ? p.q_bytes : 0u);
                     mbar_arrive_expect_tx(&full[slot], bytes);
@@ -486,8 +507,13 @@ struct DecodeKernel {
                         const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
                             (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
                         uint8_t* qdst = base + p.q_off + qs * p.q_slot_bytes;
-                        if (p.q_tma) tma_load_3d(qdst, tq, &full[slot], 0, i * p.Hq + hq0, 0);
-                        else bulk_load(qdst, qsrc, p.q_bytes, &full[slot]);
+                        if constexpr (MQ) {
+                            // rows [token][head] of QL tokens x HPC*G heads, one 4-D copy
+                            tma_load_4d(qdst, tq, &full[slot], 0, hq0, qrow_i, 0);
+                        } else {
+                            if (p.q_tma) tma_load_3d(qdst, tq, &full[slot], 0, i * p.Hq + hq0, 0);
+                            else bulk_load(qdst, qsrc, p.q_bytes, &full[slot]);
+                        }
                         ++qcount;
                     }
                 }
@@ -536,76 +562,112 @@ struct DecodeKernel {
         }
     }
 
+    // The two accumulator rows a lane owns (g4 and g4 + 8 of its 16-row
+    // tile): which query token and which head each stands for.  Tile row R
+    // of KV head hl is query token R / G, head R % G of the group; decode has
+    // one token, so R is the head.
+    struct RowInfo {
+        int j[2];          // query token index within the sequence
+        int head[2];       // query head
+        bool in[2];        // inside the group's query rows
+    };
+    static __device__ __forceinline__ RowInfo row_info(const DecodeParams& p, int hg, int hl, int mt, int lane) {
+        RowInfo ri;
+        const int rows_total = p.QL * p.G;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int R = 16 * mt + (lane >> 2) + 8 * hh;
+            const int jj = R / p.G;
+            ri.j[hh] = jj;
+            ri.head[hh] = hg * p.HPC * p.G + hl * p.G + (R - jj * p.G);
+            ri.in[hh] = R < rows_total;
+        }
+        return ri;
+    }
+    // Row of the query ring slot holding tile row R of KV head hl: the slot
+    // is [token][HPC * G heads] (one token in decode).
+    static __device__ __forceinline__ int q_smem_row(const DecodeParams& p, int hl, int R) {
+        const int jj = R / p.G;
+        return jj * p.HPC * p.G + hl * p.G + (R - jj * p.G);
+    }
+
     // End of a segment: the normalised output rows when the segment covers
     // the whole sequence (DIRECT), else the unnormalised partial (acc, m, l)
     // for the merge kernel.  Rows g4 and g4 + 8 of the tile, columns from
-    // out_col().
+    // out_col(); rows past the group or past the sequence's query tokens are
+    // not stored.
     static __device__ __forceinline__ void finish_segment(const DecodeParams& p, const StageDesc& d,
                                                           const float (&acc)[NT][4], float m0, float m1,
                                                           float l0, float l1, int lane, int rows_valid,
-                                                          int out_h0) {
+                                                          const RowInfo& ri) {
         const int g4 = lane >> 2, t4 = lane & 3;
         float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
         lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
         float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
         lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
         const bool direct = (d.flags & DIRECT) != 0;
-        if (direct || d.slot < p.max_slots) {
-            float sc0 = p.v_scale, sc1 = p.v_scale;
-            if (direct) {
-                sc0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
-                sc1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
-            }
-            QE* orow = static_cast<QE*>(p.out) + (static_cast<size_t>(d.seq) * p.Hq + out_h0) * D;
-            float* prow = p.part_acc + (static_cast<size_t>(d.slot) * p.Hq + out_h0) * D;
-            // Each lane stores 4 consecutive columns of a row per pair
-            // of column tiles.  With fp8 the permuted head_dim order
-            // already gives every lane 4 consecutive columns; otherwise
-            // one exchange between lane pairs of a quad assembles them.
+        if (!(direct || d.slot < p.max_slots)) return;
+        const int qn = static_cast<int>(d.flags >> QCOUNT_SHIFT);
+        float sc0 = p.v_scale, sc1 = p.v_scale;
+        if (direct) {
+            sc0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
+            sc1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
+        }
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                if (hh == 1 && rows_valid <= 8) break;      // rows 8..15 are padding
-                const int row = g4 + 8 * hh;
-                const float sc = hh ? sc1 : sc0;
+        for (int hh = 0; hh < 2; ++hh) {
+            if (hh == 1 && rows_valid <= 8) break;      // rows 8..15 are padding
+            const bool ok = ri.in[hh] && ri.j[hh] < qn;
+            const float sc = hh ? sc1 : sc0;
+            QE* orow = static_cast<QE*>(p.out) +
+                       (static_cast<size_t>(d.qrow0 + ri.j[hh]) * p.Hq + ri.head[hh]) * D;
+            float* prow = p.part_acc +
+                          ((static_cast<size_t>(d.slot) * p.QL + ri.j[hh]) * p.Hq + ri.head[hh]) * D;
+            // Each lane stores 4 consecutive columns of a row per pair of
+            // column tiles.  With fp8 the permuted head_dim order already
+            // gives every lane 4 consecutive columns; otherwise one exchange
+            // between lane pairs of a quad assembles them.
 #pragma unroll
-                for (int q2 = 0; q2 < NT / 2; ++q2) {
-                    const float a0 = acc[2 * q2][2 * hh] * sc, a1 = acc[2 * q2][2 * hh + 1] * sc;
-                    const float b0 = acc[2 * q2 + 1][2 * hh] * sc, b1 = acc[2 * q2 + 1][2 * hh + 1] * sc;
-                    float v[4];
-                    int col;
-                    if constexpr (FP8) {
-                        v[0] = a0; v[1] = b0; v[2] = a1; v[3] = b1;
-                        col = 16 * q2 + 4 * t4;
-                    } else {
-                        const bool odd = (t4 & 1) != 0;
-                        const float r0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
-                        const float r1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
-                        if (odd) { v[0] = r0; v[1] = r1; v[2] = b0; v[3] = b1; col = 16 * q2 + 8 + 2 * (t4 - 1); }
-                        else     { v[0] = a0; v[1] = a1; v[2] = r0; v[3] = r1; col = 16 * q2 + 2 * t4; }
-                    }
-                    if (row < rows_valid) {
-                        if (direct) store4<QE>(orow + static_cast<size_t>(row) * D + col, v);
-                        else store4<float>(prow + static_cast<size_t>(row) * D + col, v);
-                    }
+            for (int q2 = 0; q2 < NT / 2; ++q2) {
+                const float a0 = acc[2 * q2][2 * hh] * sc, a1 = acc[2 * q2][2 * hh + 1] * sc;
+                const float b0 = acc[2 * q2 + 1][2 * hh] * sc, b1 = acc[2 * q2 + 1][2 * hh + 1] * sc;
+                float v[4];
+                int col;
+                if constexpr (FP8) {
+                    v[0] = a0; v[1] = b0; v[2] = a1; v[3] = b1;
+                    col = 16 * q2 + 4 * t4;
+                } else {
+                    const bool odd = (t4 & 1) != 0;
+                    const float r0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
+                    const float r1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
+                    if (odd) { v[0] = r0; v[1] = r1; v[2] = b0; v[3] = b1; col = 16 * q2 + 8 + 2 * (t4 - 1); }
+                    else     { v[0] = a0; v[1] = a1; v[2] = r0; v[3] = r1; col = 16 * q2 + 2 * t4; }
+                }
+                if (ok) {
+                    if (direct) store4<QE>(orow + col, v);
+                    else store4<float>(prow + col, v);
                 }
             }
-            if (!direct && t4 == 0) {
-                float2* ml = p.part_ml + static_cast<size_t>(d.slot) * p.Hq;
-                if (g4 < rows_valid) ml[out_h0 + g4] = make_float2(m0, lt0);
-                if (g4 + 8 < rows_valid) ml[out_h0 + g4 + 8] = make_float2(m1, lt1);
-            }
-            if (!direct && (d.flags & GAP)) write_empty_partial(p, d.slot + 1, out_h0, rows_valid, lane);
+            if (!direct && ok && t4 == 0)
+                p.part_ml[(static_cast<size_t>(d.slot) * p.QL + ri.j[hh]) * p.Hq + ri.head[hh]] =
+                    make_float2(hh ? m1 : m0, hh ? lt1 : lt0);
         }
+        (void)g4;
     }
 
-    // An empty partial (m = -inf, l = 0, acc = 0) for `rows` query heads
-    // from out_h0 at `slot`.
-    static __device__ __forceinline__ void write_empty_partial(const DecodeParams& p, int slot, int out_h0,
-                                                               int rows, int lane) {
+    // An empty partial (m = -inf, l = 0, acc = 0) at `slot` for every query
+    // row of the warp's tile (tile rows 16*mt .. +rows).
+    static __device__ __forceinline__ void write_empty_partial(const DecodeParams& p, int slot, int hg, int hl,
+                                                               int mt, int rows, int lane) {
         if (slot >= p.max_slots) return;
-        float4* acc = reinterpret_cast<float4*>(p.part_acc + (static_cast<size_t>(slot) * p.Hq + out_h0) * D);
-        for (int e = lane; e < rows * D / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane < rows) p.part_ml[static_cast<size_t>(slot) * p.Hq + out_h0 + lane] = make_float2(-INFINITY, 0.f);
+        for (int r = 0; r < rows; ++r) {
+            const int R = 16 * mt + r;
+            const int jj = R / p.G;
+            const int head = hg * p.HPC * p.G + hl * p.G + (R - jj * p.G);
+            const size_t row = (static_cast<size_t>(slot) * p.QL + jj) * p.Hq + head;
+            float4* acc = reinterpret_cast<float4*>(p.part_acc + row * D);
+            for (int e = lane; e < D / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (lane == 0) p.part_ml[row] = make_float2(-INFINITY, 0.f);
+        }
     }
 
     // ---------------- tensor-core consumer ----------------
@@ -615,7 +677,7 @@ struct DecodeKernel {
         const int lane = threadIdx.x & 31;
         const int g4 = lane >> 2, t4 = lane & 3;
         const int hl = w / p.MT, mt = w - hl * p.MT;
-        const int rows_valid = min(16, p.G - 16 * mt);
+        const int rows_valid = min(16, p.QL * p.G - 16 * mt);
         const int S = p.stages;
         const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
                            static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
@@ -624,12 +686,12 @@ struct DecodeKernel {
         const int tokK = (mi >> 1) * 8 + r8;       // K (non-transposed) row
         const int tokV = (mi & 1) * 8 + r8;        // V (transposed) row
         const uint32_t rbK = lay.row_base(tokK, hl), rbV = lay.row_base(tokV, hl);
+        const RowInfo ri = row_info(p, hg, hl, mt, lane);
 
         float acc[NT][4];
         uint32_t qa[KS][4];
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        const int qrow_lo = hl * p.G + 16 * mt;     // first local query row of this tile
-        const int out_h0 = hg * p.HPC * p.G + qrow_lo;
+        int lim0 = INT_MAX, lim1 = INT_MAX;         // last key position each row may attend
 
         for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
             const int slot = st % S;
@@ -641,13 +703,18 @@ struct DecodeKernel {
             uint8_t* kbuf = base + slot * p.stage_bytes;
             uint8_t* vbuf = kbuf + p.kv_bytes;
             if (d.flags & SEG_START) {
-                load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo, rows_valid, lane,
-                             p.q_tma, p.HPC * p.G);
+                load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, p, hl, mt, rows_valid, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&qempty[d.qslot]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
                 m0 = m1 = -INFINITY; l0 = l1 = 0.f;
+                if constexpr (MQ) {
+                    // causal: query token j attends keys up to its own position
+                    const int qn = static_cast<int>(d.flags >> QCOUNT_SHIFT);
+                    lim0 = (ri.in[0] && ri.j[0] < qn) ? d.qpos0 + ri.j[0] : -1;
+                    lim1 = (ri.in[1] && ri.j[1] < qn) ? d.qpos0 + ri.j[1] : -1;
+                }
             }
             // V fragments of masked token rows are zeroed in registers: the
             // pool may hold NaN there and 0 * NaN would poison the sum.  A
@@ -700,7 +767,9 @@ struct DecodeKernel {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int col = nt * 8 + 2 * t4 + (e & 1);
-                    s[nt][e] = ((d.vmask >> col) & 1u) ? s[nt][e] * p.qk_scale : -INFINITY;
+                    bool keep = ((d.vmask >> col) & 1u) != 0;
+                    if constexpr (MQ) keep = keep && d.tok0 + col <= (e < 2 ? lim0 : lim1);
+                    s[nt][e] = keep ? s[nt][e] * p.qk_scale : -INFINITY;
                 }
             float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
             float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
@@ -762,7 +831,11 @@ struct DecodeKernel {
             // the producer before the segment-end epilogue.
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (d.flags & SEG_END) finish_segment(p, d, acc, m0, m1, l0, l1, lane, rows_valid, out_h0);
+            if (d.flags & SEG_END) {
+                finish_segment(p, d, acc, m0, m1, l0, l1, lane, rows_valid, ri);
+                if ((d.flags & GAP) && !(d.flags & DIRECT))
+                    write_empty_partial(p, d.slot + 1, hg, hl, mt, rows_valid, lane);
+            }
         }
     }
 
@@ -819,7 +892,8 @@ struct DecodeKernel {
         float m0 = -INFINITY, l0 = 0.f;
         float qk_scale = p.qk_scale;
         const int qrow_lo = hl * p.G;
-        const int out_h0 = hg * p.HPC * p.G + qrow_lo;
+        RowInfo ri = row_info(p, hg, hl, 0, lane);
+        ri.in[1] = false;                           // rows g4 + 8 hold the lo terms, not outputs
 
         for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
             const int slot = st % S;
@@ -935,7 +1009,9 @@ struct DecodeKernel {
                     acc[nt][0] += acc[nt][2];
                     acc[nt][1] += acc[nt][3];
                 }
-                finish_segment(p, d, acc, m0, -INFINITY, l0, 0.f, lane, rows_valid, out_h0);
+                finish_segment(p, d, acc, m0, -INFINITY, l0, 0.f, lane, rows_valid, ri);
+                if ((d.flags & GAP) && !(d.flags & DIRECT))
+                    write_empty_partial(p, d.slot + 1, hg, hl, 0, rows_valid, lane);
             }
         }
     }
@@ -1010,9 +1086,11 @@ struct DecodeKernel {
     // A fragments of this tile's query rows (16 x D) from the stage's query
     // copy; rows past the group are zero.
     static __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[KS][4], const uint8_t* qbuf,
-                                                        int qrow_lo, int rows_valid, int lane,
-                                                        int q_tma, int qrows) {
+                                                        const DecodeParams& p, int hl, int mt,
+                                                        int rows_valid, int lane) {
         const int g4 = lane >> 2, t4 = lane & 3;
+        const int q_tma = p.q_tma;
+        const int qrows = p.HPC * p.G * p.QL;       // rows of one 128-B column plane of the slot
         // byte offset of 16-byte column chunk c of query row r in the ring
         // slot: [column block][row][128 B] with the 128-B swizzle when the
         // rows came by tensor copy, plain row-major otherwise
@@ -1027,16 +1105,18 @@ struct DecodeKernel {
             const int mi = lane >> 3, r8 = lane & 7;
             int row = (mi & 1) * 8 + r8;
             if (row >= rows_valid) row = 0;
+            const int srow = q_smem_row(p, hl, 16 * mt + row);
             const uint32_t qb = smem_u32(qbuf);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                ldsm_x4(qb + qaddr(qrow_lo + row, 2 * ks + (mi >> 1)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+                ldsm_x4(qb + qaddr(srow, 2 * ks + (mi >> 1)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
             }
         } else {
             // head_dim order inside a 16-wide k-step is permuted to match the
             // byte order of e4m3 key rows: logical k (2t, 2t+1, 2t+8, 2t+9)
             // holds physical dims (4t, 4t+1, 4t+2, 4t+3).
-            const int r0 = qrow_lo + min(g4, rows_valid - 1), r1 = qrow_lo + min(g4 + 8, rows_valid - 1);
+            const int r0 = q_smem_row(p, hl, 16 * mt + min(g4, rows_valid - 1));
+            const int r1 = q_smem_row(p, hl, 16 * mt + min(g4 + 8, rows_valid - 1));
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int c = 2 * ks + (t4 >> 1), inner = 8 * (t4 & 1);
@@ -1196,7 +1276,7 @@ struct DecodeKernel {
                             if (lane == 0) ml[out_h0 + r] = make_float2(m[r], l[r]);
                         }
                     }
-                    if (d.flags & GAP) write_empty_partial(p, d.slot + 1, out_h0, nr, lane);
+                    if (d.flags & GAP) write_empty_partial(p, d.slot + 1, hg, hl, mt, nr, lane);
                 }
             }
             __syncwarp();
@@ -1246,11 +1326,11 @@ struct DecodeKernel {
     }
 };
 
-template <class KV, class QT, int D, bool TC, int CT>
+template <class KV, class QT, int D, bool TC, int CT, bool MQ = false>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
-    using K = DecodeKernel<KV, QT, D, TC, CT>;
+    using K = DecodeKernel<KV, QT, D, TC, CT, MQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + p.bar_off);
@@ -1347,15 +1427,26 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = warp % WPI;
     const int HG = cdiv_i(p.Hq, HPB);    // head groups of HPB heads
+    const int per_seq = p.QL * HG;       // items of one split sequence: query tokens x head groups
     grid_dependency_wait();
     for (int item = blockIdx.x;; item += gridDim.x) {
         // the count and this item's list entry load together
         const int count = *reinterpret_cast<volatile int*>(&p.totals[2]);
-        const int4 e = p.split_list[min(item / HG, p.B - 1)];
-        if (item >= count * HG) break;
+        const int4 e = p.split_list[min(item / per_seq, p.B - 1)];
+        if (item >= count * per_seq) break;
+        const int jq = (item / HG) % p.QL;                // query token of the sequence
         const int h = (item % HG) * HPB + warp / WPI;
         if (WPI == 1 && h >= p.Hq) continue;
-        OutT* o = static_cast<OutT*>(p.out) + (static_cast<size_t>(e.x) * p.Hq + h) * D + lane * DPL;
+        int qrow = e.x;                                   // row of (sequence, token) in q / out
+        if (p.q_start) {
+            const int a = p.q_start[e.x];
+            if (jq >= p.q_start[e.x + 1] - a) continue;   // the sequence has fewer query tokens
+            qrow = a + jq;
+        }
+        // partial rows of this (token, head): slot * QL * Hq + jq * Hq + h
+        const size_t prow0 = static_cast<size_t>(jq) * p.Hq + h;
+        const size_t pstride = static_cast<size_t>(p.QL) * p.Hq;
+        OutT* o = static_cast<OutT*>(p.out) + (static_cast<size_t>(qrow) * p.Hq + h) * D + lane * DPL;
         float num[DPL];
 #pragma unroll
         for (int c = 0; c < DPL; ++c) num[c] = 0.f;
@@ -1369,13 +1460,13 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
             for (int t = 0; t < NB; ++t) {
                 const int st = __shfl_sync(0xffffffffu, my_slot, t);
                 if (t < n) {
-                    VecF<DPL>::load(p.part_acc + (static_cast<size_t>(st) * p.Hq + h) * D + lane * DPL, v[t]);
+                    VecF<DPL>::load(p.part_acc + (static_cast<size_t>(st) * pstride + prow0) * D + lane * DPL, v[t]);
                 } else {
 #pragma unroll
                     for (int c = 0; c < DPL; ++c) v[t][c] = 0.f;
                 }
             }
-            const float2 ml = lane < n ? ldg_f2(p.part_ml + static_cast<size_t>(my_slot) * p.Hq + h)
+            const float2 ml = lane < n ? ldg_f2(p.part_ml + static_cast<size_t>(my_slot) * pstride + prow0)
                                        : make_float2(-INFINITY, 0.f);
             float bm = ml.x;
 #pragma unroll
