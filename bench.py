@@ -255,12 +255,24 @@ def run_ours(args, rank, world, local) -> dict | None:
     wl = make_workload(args.workload, 1, device)
     d = wl.to(device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
+    fill = None
     for kind, payload in d.setup:
         if kind == "copy":
             pa.pa_copy_blocks(d.k_cache, d.v_cache, payload, err_flag=err)
         else:
+            # the pool's history arrives through the cache write: time the large fills
+            fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            fa.record()
             pa.pa_reshape_and_cache(d.k_cache, d.v_cache, payload.key, payload.value, payload.slots,
                                     k_scale=d.k_scale, v_scale=d.v_scale, err_flag=err)
+            fb.record()
+            torch.cuda.synchronize()
+            T = payload.slots.numel()
+            if T >= 100000:
+                nbytes = T * wl.num_kv_heads * wl.head_dim * 2 * (payload.key.element_size() +
+                                                                  sizing.ELEM_BYTES[wl.kv_dtype])
+                fill = {"tokens": T, "us": fa.elapsed_time(fb) * 1e3,
+                        "gbs": nbytes / (fa.elapsed_time(fb) / 1e3) / 1e9}
     out = torch.empty_like(d.q)
     MB = d.block_tables.shape[1]
     ws = pa.alloc_workspace(d.num_seqs, d.num_q_heads, d.head_dim, MB * d.block_size, args.partition_tokens,
@@ -308,10 +320,16 @@ def run_ours(args, rank, world, local) -> dict | None:
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.start()
     t_start.record(stream)
+    ew = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         if pairs is not None:
+            ec[i][0].record(stream)
             pa.pa_copy_blocks(d.k_cache, d.v_cache, pairs, err_flag=err)
+            ec[i][1].record(stream)
+        ew[i][0].record(stream)
         write(d.q, d.new_key, d.new_value, d.slot_mapping)
+        ew[i][1].record(stream)
         ev[i][0].record(stream)
         decode(d.q, d.block_tables, d.seq_lens, out)
         ev[i][1].record(stream)
@@ -322,6 +340,8 @@ def run_ours(args, rank, world, local) -> dict | None:
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    write_us = statistics.mean(a.elapsed_time(b) for a, b in ew) * 1e3
+    copy_us = statistics.mean(a.elapsed_time(b) for a, b in ec) * 1e3 if pairs is not None else None
     t = torch.tensor([ms_total, dec_ms], dtype=torch.float64, device=device)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -393,7 +413,12 @@ def run_ours(args, rank, world, local) -> dict | None:
                         "launch_ms": dec_ms,
                         "traffic": profile_traffic(args.workload) if NQ == 1 and not args.partition_tokens else None},
            "gpu_launches": K * (3 + (1 if pairs is not None else 0)),
-           "clocks": clk, "e2e": e2e}
+           "clocks": clk, "e2e": e2e,
+           "cache_write_us_per_step": write_us,
+           "copy_blocks_us_per_step": copy_us,
+           "copy_blocks_pairs": int(pairs.shape[0]) if pairs is not None else 0}
+    if fill is not None:
+        res["cache_fill"] = fill
     if not args.no_cpu_baseline and world == 1:
         rate, n, el = time_oracle(wl.to("cpu"), budget_s=args.cpu_budget)
         res["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",

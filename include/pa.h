@@ -117,7 +117,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
  * Precision: scores and sums accumulate in fp32.  The probabilities enter
  * P*V rounded to the MMA operand type: bf16 (8 significant bits) for bf16
  * caches, f16 (11 bits) for f16 caches and fp8 caches on 16-token chunks.
- * On the fp8 32-token path the query and the probabilities are each carried
+ * On the fp8 32-token path (e4m3 and e5m2 caches: the key and value bytes
+ * are MMA operands as stored) the query and the probabilities are each carried
  * as two e4m3 terms, 8 significant bits (exact for bf16 queries, except
  * elements below 2^-9 of the largest in their GQA group); an infinite query
  * element saturates to +-448 there instead of propagating.  pa_decode_simt

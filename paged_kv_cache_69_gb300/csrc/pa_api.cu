@@ -184,11 +184,11 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     // fp8 caches on the tensor-core path run the native-e4m3 kernel (32-token
     // chunks, GQA groups of up to 8 heads, partitions a multiple of 32
     // tokens); other fp8 shapes convert e4m3 to f16 in registers.
-    const bool native8 = !mq && tc && kv_dtype == PA_FP8_E4M3 && D == 128 && Hq / Hkv <= 8 &&
+    const bool native8 = !mq && tc && is_fp8(kv_dtype) && D == 128 && Hq / Hkv <= 8 &&
                          partition_tokens % 32 == 0;
     const int CT = native8 ? 32 : 16;
     const void* kern = mq      ? decode_kernel_mq(kv_dtype, q_dtype, D)
-                       : native8 ? decode_kernel_e4m3(q_dtype, D)
+                       : native8 ? decode_kernel_e4m3(kv_dtype, q_dtype, D)
                        : tc    ? decode_kernel_tc(kv_dtype, q_dtype, D)
                                : decode_kernel_simt(kv_dtype, q_dtype, D);
     if (!kern) return fail(PA_ERR_UNSUPPORTED, "decode: no kernel for this dtype / head_dim combination");

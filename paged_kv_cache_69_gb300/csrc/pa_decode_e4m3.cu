@@ -1,6 +1,7 @@
-// pa_decode_e4m3.cu -- native-e4m3 tensor-core instantiations of the paged
+// pa_decode_e4m3.cu -- native-fp8 tensor-core instantiations of the paged
 // decode kernel (fp8 caches, head_dim 128, 32-token chunks, mma.sync
-// m16n8k32 with e4m3 operands and fp32 accumulation).
+// m16n8k32: e4m3 query / probability terms times e4m3 or e5m2 K/V bytes,
+// fp32 accumulation).
 #include <cuda.h>
 
 #include "pa_decode_kernel.cuh"
@@ -8,10 +9,16 @@
 
 namespace pa {
 
-const void* decode_kernel_e4m3(pa_dtype q, int D) {
+const void* decode_kernel_e4m3(pa_dtype kv, pa_dtype q, int D) {
     if (D != 128) return nullptr;
-    if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, true, 32>);
-    if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, true, 32>);
+    if (kv == PA_FP8_E4M3) {
+        if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, F16T, 128, true, 32>);
+        if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<FP8T, BF16T, 128, true, 32>);
+    }
+    if (kv == PA_FP8_E5M2) {
+        if (q == PA_F16) return reinterpret_cast<const void*>(&pa_decode_kernel<E5M2T, F16T, 128, true, 32>);
+        if (q == PA_BF16) return reinterpret_cast<const void*>(&pa_decode_kernel<E5M2T, BF16T, 128, true, 32>);
+    }
     return nullptr;
 }
 

@@ -335,8 +335,8 @@ struct DecodeKernel {
     // 32-token chunks are the native-e4m3 tensor-core variant (fp8 operands,
     // m16n8k32); every other variant runs 16-token chunks.
     static constexpr bool NATIVE8 = (CT == 32);
-    static_assert(CT == 16 || (CT == 32 && KV::code == PA_FP8_E4M3 && TC && D == 128),
-                  "32-token chunks: e4m3 tensor-core path only");
+    static_assert(CT == 16 || (CT == 32 && FP8 && TC && D == 128), "32-token chunks: fp8 tensor-core path only");
+    static constexpr bool KV_E5M2 = (KV::code == PA_FP8_E5M2);
     static constexpr int MAXB = CT / 8;       // TMA boxes per chunk at the smallest block size
     static constexpr bool MMA_BF16 = (KV::code == PA_BF16);   // fp8 runs in f16
     static constexpr int NT = D / 8;          // 8-wide output column tiles
@@ -923,10 +923,10 @@ struct DecodeKernel {
                 uint32_t r0, r1, r2, r3, c0, c1, c2, c3;
                 ldsm_x4(kb + lay.chunk_addr(rbK0, tokK, 2 * ks + (mi & 1)), r0, r1, r2, r3);
                 ldsm_x4(kb + lay.chunk_addr(rbK1, tokK, 2 * ks + (mi & 1)), c0, c1, c2, c3);
-                mma_e4m3_16832(s[0], qa[ks], r0, r1);
-                mma_e4m3_16832(s[1], qa[ks], r2, r3);
-                mma_e4m3_16832(s[2], qa[ks], c0, c1);
-                mma_e4m3_16832(s[3], qa[ks], c2, c3);
+                mma_e4m3_16832<KV_E5M2>(s[0], qa[ks], r0, r1);
+                mma_e4m3_16832<KV_E5M2>(s[1], qa[ks], r2, r3);
+                mma_e4m3_16832<KV_E5M2>(s[2], qa[ks], c0, c1);
+                mma_e4m3_16832<KV_E5M2>(s[3], qa[ks], c2, c3);
             }
             // ---- online softmax (log2 domain) of row g4 over 8 tokens per lane ----
             float x[4][2];
@@ -994,8 +994,8 @@ struct DecodeKernel {
                     if constexpr (decltype(masked)::value) {
                         e0 &= mk0; o0 &= mk0; e1 &= mk1; o1 &= mk1;
                     }
-                    mma_e4m3_16832(acc[2 * c], pa, e0, e1);
-                    mma_e4m3_16832(acc[2 * c + 1], pa, o0, o1);
+                    mma_e4m3_16832<KV_E5M2>(acc[2 * c], pa, e0, e1);
+                    mma_e4m3_16832<KV_E5M2>(acc[2 * c + 1], pa, o0, o1);
                 }
             };
             if (d.vmask == 0xffffffffu) pv(std::false_type{});      // every token of the chunk is valid

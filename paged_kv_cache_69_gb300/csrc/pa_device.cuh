@@ -207,12 +207,22 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_bytes) {
 // registers of four bytes (row g, k 4t..4t+3 | row g+8, same k | row g,
 // k 16+4t.. | row g+8, k 16+4t..); B holds 32 k x 8 columns as two registers
 // (column g, k 4t..4t+3 | k 16+4t..), with g = lane / 4, t = lane % 4.
+template <bool B_E5M2 = false>
 __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    if constexpr (B_E5M2) {
+        // A in e4m3, B in e5m2 (the fp8 element types of A and B are independent)
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e5m2.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
 }
 
 // Two floats to two e4m3 bytes (lo -> low byte), round to nearest even,

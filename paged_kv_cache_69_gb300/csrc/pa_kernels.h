@@ -7,8 +7,8 @@ namespace pa {
 // Kernel entry for the given cache dtype, query dtype and head_dim, or null.
 const void* decode_kernel_tc(pa_dtype kv, pa_dtype q, int D);
 const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D);
-// fp8-e4m3 cache, tensor cores with e4m3 operands, 32-token chunks.
-const void* decode_kernel_e4m3(pa_dtype q, int D);
+// fp8 cache (e4m3 or e5m2), tensor cores with fp8 operands, 32-token chunks.
+const void* decode_kernel_e4m3(pa_dtype kv, pa_dtype q, int D);
 // several (causal) query tokens per sequence, tensor cores.
 const void* decode_kernel_mq(pa_dtype kv, pa_dtype q, int D);
 // Log-sum-exp merge; split_heads: several warps per (sequence, head), for
