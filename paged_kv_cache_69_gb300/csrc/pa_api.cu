@@ -187,7 +187,9 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     const bool native8 = !mq && tc && is_fp8(kv_dtype) && D == 128 && Hq / Hkv <= 8 &&
                          partition_tokens % 32 == 0;
     const int CT = native8 ? 32 : 16;
+    const bool fp8t = native8 && Hq / Hkv <= 4;      // keys as the MMA rows: half the MMAs
     const void* kern = mq      ? decode_kernel_mq(kv_dtype, q_dtype, D)
+                       : fp8t  ? decode_kernel_fp8t(kv_dtype, q_dtype, D)
                        : native8 ? decode_kernel_e4m3(kv_dtype, q_dtype, D)
                        : tc    ? decode_kernel_tc(kv_dtype, q_dtype, D)
                                : decode_kernel_simt(kv_dtype, q_dtype, D);
@@ -241,7 +243,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.q_bytes = static_cast<uint32_t>(QL * HPC * G * D * eq);
     p.q_slot_bytes = (p.q_bytes + 1023u) & ~1023u;   // swizzled tensor copies need 1024-B alignment
     p.stage_bytes = 2 * p.kv_bytes;
-    const uint32_t simtq = tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
+    // CUDA-core variant: private fp32 query rows; transposed fp8: P bytes per warp
+    const uint32_t simtq = fp8t ? static_cast<uint32_t>(NCW * 256) : tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
     const uint32_t extras = 1024;   // barriers, stage descriptors, prologue scratch
     const uint32_t fixed = NQ * p.q_slot_bytes + simtq + extras + 1024;   // + base alignment slack
     const int threads = (NCW + 1) * 32;

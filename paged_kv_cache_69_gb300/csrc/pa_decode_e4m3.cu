@@ -22,4 +22,13 @@ const void* decode_kernel_e4m3(pa_dtype kv, pa_dtype q, int D) {
     return nullptr;
 }
 
+const void* decode_kernel_fp8t(pa_dtype kv, pa_dtype q, int D) {
+#define PA_T8(KVT, QTT) reinterpret_cast<const void*>(&pa_decode_kernel<KVT, QTT, 128, true, 32, false, true>)
+    if (D != 128) return nullptr;
+    if (kv == PA_FP8_E4M3) return q == PA_F16 ? PA_T8(FP8T, F16T) : q == PA_BF16 ? PA_T8(FP8T, BF16T) : nullptr;
+    if (kv == PA_FP8_E5M2) return q == PA_F16 ? PA_T8(E5M2T, F16T) : q == PA_BF16 ? PA_T8(E5M2T, BF16T) : nullptr;
+#undef PA_T8
+    return nullptr;
+}
+
 }  // namespace pa

@@ -327,7 +327,7 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16*
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v[0], v[1], true), pack2(v[2], v[3], true));
 }
 
-template <class KV, class QT, int D, bool TC, int CT, bool MQ = false>
+template <class KV, class QT, int D, bool TC, int CT, bool MQ = false, bool T8 = false>
 struct DecodeKernel {
     using KT = typename KV::T;
     using QE = typename QT::T;
@@ -1016,6 +1016,242 @@ struct DecodeKernel {
         }
     }
 
+    // ---------------- transposed native-fp8 consumer (GQA groups of <= 4) ----------------
+    // Keys are the M rows of the first product, S^T = K Q^T, with the 2G
+    // query columns (the hi and the lo term of each head) as N = 8; the
+    // second is O^T = V^T P^T with 16 head-dim rows per tile.  Each product
+    // takes half the MMAs of the packed layout.  A lane owns one head (t4) in
+    // both products, so its softmax statistics rescale its own accumulators.
+    // P reaches the B layout of the second product through 256 bytes of
+    // shared memory per warp.
+    static __device__ void consumer_fp8t(const DecodeParams& p, const Plan& pl, int hg, int w,
+                                         uint8_t* base, uint64_t* full, uint64_t* empty, uint64_t* qempty,
+                                         const StageDesc* descs, uint8_t* pt) {
+        const int lane = threadIdx.x & 31;
+        const int g4 = lane >> 2, t4 = lane & 3;
+        const int hl = w;                           // one warp per KV head
+        const int S = p.stages;
+        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
+                           static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
+        const int mi = lane >> 3, r8 = lane & 7;
+        // K as A: matrix mi holds tokens (mi & 1) * 8 .. of the k-half mi >> 1
+        const int tokA = (mi & 1) * 8 + r8;
+        const uint32_t rbK0 = lay.row_base(tokA, hl), rbK1 = lay.row_base(tokA + 16, hl);
+        // V transposed as A: matrix mi holds tokens 8 mi ..
+        const int tokV = mi * 8 + r8;
+        const uint32_t rbV = lay.row_base(tokV, hl);
+        uint8_t* ptw = pt + w * 256;                // [8 columns][32 logical k] bytes
+        const bool head_ok = t4 < p.G;
+        const int head = hg * p.HPC * p.G + hl * p.G + t4;
+        // logical k of this lane's hi/lo words: even g4 = 2m fills k 4m..4m+3,
+        // odd g4 = 2m+1 fills k 16+4m..16+4m+3
+        const int kblk = (g4 & 1) ? 16 + 4 * (g4 >> 1) : 4 * (g4 >> 1);
+
+        float acc[8][4];
+        uint32_t qb[KS8][2];
+        float m = -INFINITY, l = 0.f;
+        float qk_scale = p.qk_scale;
+
+        for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
+            const int slot = st % S;
+            if (!mbar_wait_bounded(&full[slot], (st / S) & 1u)) {
+                if (lane == 0) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+                return;
+            }
+            const StageDesc d = descs[slot];
+            uint8_t* kbuf = base + slot * p.stage_bytes;
+            uint8_t* vbuf = kbuf + p.kv_bytes;
+            if (d.flags & SEG_START) {
+                qk_scale = p.qk_scale * load_q_fp8t(qb, base + p.q_off + d.qslot * p.q_slot_bytes, hl * p.G,
+                                                     p.G, lane, p.q_tma, p.HPC * p.G);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+                m = -INFINITY; l = 0.f;
+            }
+            // ---- S^T = K Q^T: tokens 0-15 and 16-31 x 8 query columns ----
+            float s[2][4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+            const uint32_t kb = smem_u32(kbuf);
+#pragma unroll
+            for (int ks = 0; ks < KS8; ++ks) {
+                uint32_t a[4], b[4];
+                ldsm_x4(kb + lay.chunk_addr(rbK0, tokA, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                ldsm_x4(kb + lay.chunk_addr(rbK1, tokA, 2 * ks + (mi >> 1)), b[0], b[1], b[2], b[3]);
+                mma_fp8_16832<KV_E5M2, false>(s[0], a, qb[ks][0], qb[ks][1]);
+                mma_fp8_16832<KV_E5M2, false>(s[1], b, qb[ks][0], qb[ks][1]);
+            }
+            // ---- online softmax of head t4 over its tokens g4, g4+8, 16+g4, 24+g4 ----
+            float x[4];
+            x[0] = s[0][0] + s[0][1];       // hi + lo columns of the head
+            x[1] = s[0][2] + s[0][3];
+            x[2] = s[1][0] + s[1][1];
+            x[3] = s[1][2] + s[1][3];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int tok = (a & 1) * 8 + (a >> 1) * 16 + g4;
+                x[a] = ((d.vmask >> tok) & 1u) ? x[a] * qk_scale : -INFINITY;
+            }
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m, mx);
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            const float al = exp2f(m - mu);
+            m = mn;
+            const float eb = mu - 8.f;                 // weights scaled by 2^8
+            float pr[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) pr[a] = exp2f(x[a] - eb);
+            l = l * al + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+            if (!__all_sync(0xffffffffu, al == 1.f)) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    acc[c][0] *= al; acc[c][1] *= al; acc[c][2] *= al; acc[c][3] *= al;
+                }
+            }
+            // ---- P^T to the B layout through shared memory ----
+            uint32_t h01, l01, h23, l23;
+            split_e4m3x2(pr[0], pr[1], h01, l01);
+            split_e4m3x2(pr[2], pr[3], h23, l23);
+            const uint32_t myhi = h01 | (h23 << 16), mylo = l01 | (l23 << 16);   // bytes: tokens g4, g4+8, 16+g4, 24+g4
+            const uint32_t ohi = __shfl_xor_sync(0xffffffffu, myhi, 4);         // partner g4 ^ 1
+            const uint32_t olo = __shfl_xor_sync(0xffffffffu, mylo, 4);
+            // even g4 = 2m: tokens (2m, 2m+1, 2m+8, 2m+9) = (own, partner, own, partner) of bytes 0, 1;
+            // odd g4: tokens 16 + (2m, 2m+1, 2m+8, 2m+9) = (partner, own, partner, own) of bytes 2, 3
+            const uint32_t sel = (g4 & 1) ? 0x3726u : 0x5140u;
+            const uint32_t whi = __byte_perm(myhi, ohi, sel), wlo = __byte_perm(mylo, olo, sel);
+            __syncwarp();                               // the previous chunk's reads are done
+            *reinterpret_cast<uint32_t*>(ptw + (2 * t4) * 32 + kblk) = whi;
+            *reinterpret_cast<uint32_t*>(ptw + (2 * t4 + 1) * 32 + kblk) = wlo;
+            __syncwarp();
+            const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(ptw + g4 * 32 + 4 * t4);
+            const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(ptw + g4 * 32 + 16 + 4 * t4);
+            // ---- O^T += V^T P^T: 8 tiles of 16 head-dim rows (dims 16c + 2r, 16c + 2r + 1) ----
+            const uint32_t vb = smem_u32(vbuf);
+            auto pv = [&](auto masked) {
+                uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+                if constexpr (decltype(masked)::value) {
+                    mk0 = token_bytemask(d.vmask >> (2 * t4));
+                    mk1 = token_bytemask(d.vmask >> (16 + 2 * t4));
+                }
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t r0, r1, r2, r3;     // tokens 0-7, 8-15, 16-23, 24-31 of column chunk c
+                    ldsm_x4_t(vb + lay.chunk_addr(rbV, tokV, c), r0, r1, r2, r3);
+                    uint32_t a[4] = {__byte_perm(r0, r1, 0x6420), __byte_perm(r0, r1, 0x7531),
+                                     __byte_perm(r2, r3, 0x6420), __byte_perm(r2, r3, 0x7531)};
+                    if constexpr (decltype(masked)::value) {
+                        a[0] &= mk0; a[1] &= mk0; a[2] &= mk1; a[3] &= mk1;
+                    }
+                    mma_fp8_16832<KV_E5M2, false>(acc[c], a, pb0, pb1);
+                }
+            };
+            if (d.vmask == 0xffffffffu) pv(std::false_type{});
+            else pv(std::true_type{});
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (d.flags & SEG_END) {
+                float lt = l + __shfl_xor_sync(0xffffffffu, l, 4);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+                const bool direct = (d.flags & DIRECT) != 0;
+                if (direct || d.slot < p.max_slots) {
+                    const float sc = direct ? (lt > 0.f ? p.v_scale / lt : 0.f) : p.v_scale;
+                    if (head_ok) {
+                        const size_t row = static_cast<size_t>(d.qrow0) * p.Hq + head;
+                        QE* orow = static_cast<QE*>(p.out) + row * D;
+                        float* prow = p.part_acc + (static_cast<size_t>(d.slot) * p.QL * p.Hq + head) * D;
+#pragma unroll
+                        for (int c = 0; c < D / 16; ++c) {
+                            const float v0 = (acc[c][0] + acc[c][1]) * sc;    // dim 16c + 2 g4
+                            const float v1 = (acc[c][2] + acc[c][3]) * sc;    // dim 16c + 2 g4 + 1
+                            const int col = 16 * c + 2 * g4;
+                            if (direct) {
+                                store_pair(orow + col, v0, v1);
+                            } else {
+                                *reinterpret_cast<float2*>(prow + col) = make_float2(v0, v1);
+                            }
+                        }
+                        if (!direct && g4 == 0)
+                            p.part_ml[static_cast<size_t>(d.slot) * p.QL * p.Hq + head] = make_float2(m, lt);
+                    }
+                    if (!direct && (d.flags & GAP)) write_empty_partial(p, d.slot + 1, hg, hl, 0, p.G, lane);
+                }
+            }
+        }
+    }
+
+    // The query as the B fragments of S^T = K Q^T: column g4 is the hi
+    // (g4 even) or lo (g4 odd) e4m3 term of head g4 / 2 of the group, for
+    // head dims 32ks + 4t4 .. +3 (register 0) and 16 more (register 1); heads
+    // past the group are zero.  Returns 2^-e, the inverse of the tile scale.
+    static __device__ __forceinline__ float load_q_fp8t(uint32_t (&qb)[KS8][2], const uint8_t* qbuf, int qrow_lo,
+                                                        int G, int lane, int q_tma, int qrows) {
+        const int g4 = lane >> 2, t4 = lane & 3;
+        auto qaddr = [&](int r, int c) -> uint32_t {
+            if (q_tma) {
+                const int rr = (c >> 3) * qrows + r;
+                return static_cast<uint32_t>(rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
+            }
+            return static_cast<uint32_t>(r * D * 2 + c * 16);
+        };
+        const int h = g4 >> 1;
+        const int row = qrow_lo + min(h, G - 1);
+        auto load4 = [&](int ks, int hk, float (&f)[4]) {
+            const int c = 4 * ks + 2 * hk + (t4 >> 1);
+            const uint2 u = *reinterpret_cast<const uint2*>(qbuf + qaddr(row, c) + 8 * (t4 & 1));
+            float2 f0, f1;
+            if constexpr (QT::code == PA_F16) {
+                f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+                f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            } else {
+                f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+                f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+            }
+            f[0] = f0.x; f[1] = f0.y; f[2] = f1.x; f[3] = f1.y;
+        };
+        float mx = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) {
+                float f[4];
+                load4(ks, hk, f);
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
+            }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int e = 0;
+        if (mx > 0.f && mx <= 3.0e38f) {
+            const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;   // floor(log2(mx))
+            e = max(-60, min(60, 7 - ex));
+        }
+        const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+        const bool lo_term = (g4 & 1) != 0, pad = h >= G;
+#pragma unroll
+        for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) {
+                float f[4];
+                load4(ks, hk, f);
+                const float a0 = f[0] * sc, a1 = f[1] * sc, a2 = f[2] * sc, a3 = f[3] * sc;
+                uint32_t v01 = f32x2_to_e4m3x2(a0, a1), v23 = f32x2_to_e4m3x2(a2, a3);
+                if (lo_term) {
+                    const uint32_t f01 = e4m3x2_to_f16x2(v01), f23 = e4m3x2_to_f16x2(v23);
+                    const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
+                    const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
+                    v01 = f32x2_to_e4m3x2(a0 - b01.x, a1 - b01.y);
+                    v23 = f32x2_to_e4m3x2(a2 - b23.x, a3 - b23.y);
+                }
+                qb[ks][hk] = pad ? 0u : (v01 | (v23 << 16));
+            }
+        return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    }
+
     // The query tile as A fragments (m16n8k32 layout, head_dim in natural
     // order): row g4 < G holds e4m3(2^e q) and row g4 + 8 the e4m3 residual;
     // rows past the group are zero.  Returns 2^-e.
@@ -1326,11 +1562,11 @@ struct DecodeKernel {
     }
 };
 
-template <class KV, class QT, int D, bool TC, int CT, bool MQ = false>
+template <class KV, class QT, int D, bool TC, int CT, bool MQ = false, bool T8 = false>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
-    using K = DecodeKernel<KV, QT, D, TC, CT, MQ>;
+    using K = DecodeKernel<KV, QT, D, TC, CT, MQ, T8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + p.bar_off);
@@ -1371,7 +1607,9 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         }
         K::producer(p, pl, hg, base, full, empty, qempty, descs, &tk, &tv, &tq);
     } else if (warp < p.NCW) {
-        if constexpr (K::NATIVE8) {
+        if constexpr (T8) {
+            K::consumer_fp8t(p, pl, hg, warp, base, full, empty, qempty, descs, base + p.simtq_off);
+        } else if constexpr (K::NATIVE8) {
             K::consumer_e4m3(p, pl, hg, warp, base, full, empty, qempty, descs);
         } else if constexpr (TC) {
             K::consumer_tc(p, pl, hg, warp, base, full, empty, qempty, descs);

@@ -225,6 +225,27 @@ __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a
     }
 }
 
+// D += A B, m16n8k32, fp8 A and B with independent formats (A: e4m3 or e5m2,
+// B: e4m3 or e5m2), fp32 accumulator; fragment layout as mma_e4m3_16832.
+template <bool A_E5M2, bool B_E5M2>
+__device__ __forceinline__ void mma_fp8_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (A_E5M2 && !B_E5M2) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.f32.e5m2.e4m3.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else if constexpr (!A_E5M2) {
+        mma_e4m3_16832<B_E5M2>(d, a, b0, b1);
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.f32.e5m2.e5m2.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
 // Two floats to two e4m3 bytes (lo -> low byte), round to nearest even,
 // saturating to +-448 (PTX ISA: cvt, .e4m3x2 destination).
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {

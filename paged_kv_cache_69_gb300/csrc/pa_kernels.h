@@ -9,6 +9,8 @@ const void* decode_kernel_tc(pa_dtype kv, pa_dtype q, int D);
 const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D);
 // fp8 cache (e4m3 or e5m2), tensor cores with fp8 operands, 32-token chunks.
 const void* decode_kernel_e4m3(pa_dtype kv, pa_dtype q, int D);
+// the same for GQA groups of at most 4 heads: keys as the MMA rows.
+const void* decode_kernel_fp8t(pa_dtype kv, pa_dtype q, int D);
 // several (causal) query tokens per sequence, tensor cores.
 const void* decode_kernel_mq(pa_dtype kv, pa_dtype q, int D);
 // Log-sum-exp merge; split_heads: several warps per (sequence, head), for
