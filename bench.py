@@ -109,6 +109,22 @@ def profile_traffic(workload: str):
 # ---------------------------------------------------------------------------
 # clocks during the timed region (NVML read-only queries)
 # ---------------------------------------------------------------------------
+def capture_graph(fn):
+    """fn's launches captured as one CUDA graph, or None (with a note on
+    stderr) when capture fails; the eager launches are then timed instead."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            fn()
+        torch.cuda.synchronize()
+        return g
+    except Exception as e:  # noqa: BLE001 -- any capture failure falls back to eager timing
+        torch.cuda.synchronize()
+        print(f"bench: CUDA graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        return None
+
+
 class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
@@ -312,6 +328,9 @@ def run_ours(args, rank, world, local) -> dict | None:
     for _ in range(args.warmup):
         step(*dev_args)
     torch.cuda.synchronize()
+    # The step as one CUDA graph: replaying it keeps host launch gaps out of
+    # the step time (the kernels and their order are those of the eager step).
+    graph = None if args.eager else capture_graph(lambda: step(*dev_args))
     if world > 1:
         dist.barrier()
     clocks = ClockSampler(local)
@@ -322,6 +341,25 @@ def run_ours(args, rank, world, local) -> dict | None:
     t_start.record(stream)
     ew = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if graph is not None:
+        # K steps replayed back to back: the step time
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t_start.record(stream)
+        for _ in range(K):
+            graph.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        g_start, g_end = t_start, t_end
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+    # K eager steps with events around each kernel: the per-kernel times
+    # (and the step time when no graph is used)
     for i in range(K):
         if pairs is not None:
             ec[i][0].record(stream)
@@ -338,7 +376,7 @@ def run_ours(args, rank, world, local) -> dict | None:
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = g_start.elapsed_time(g_end) if graph is not None else t_start.elapsed_time(t_end)
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     write_us = statistics.mean(a.elapsed_time(b) for a, b in ew) * 1e3
     copy_us = statistics.mean(a.elapsed_time(b) for a, b in ec) * 1e3 if pairs is not None else None
@@ -369,12 +407,17 @@ def run_ours(args, rank, world, local) -> dict | None:
         for _ in range(args.warmup):
             e2e_step()
         torch.cuda.synchronize()
+        g_e2e = None if args.eager else capture_graph(e2e_step)
+        run_e2e = g_e2e.replay if g_e2e is not None else e2e_step
+        for _ in range(args.warmup):
+            run_e2e()
+        torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(K):
-            e2e_step()
+            run_e2e()
         b.record(stream)
         torch.cuda.synchronize()
         te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device=device)
@@ -404,6 +447,7 @@ def run_ours(args, rank, world, local) -> dict | None:
                                           "decode_variant": "cuda-core" if args.simt else "tensor-core",
                                           "partition_tokens": args.partition_tokens,
                                           "query_tokens_per_seq": NQ,
+                                          "launch": "cuda_graph" if graph is not None else "eager",
                                           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
            "kv_gbs": achieved, "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -564,6 +608,7 @@ def main():
     ap.add_argument("--q-per-seq", type=int, default=1,
                     help="query tokens per sequence (>1: speculative-decoding step through pa_attention)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time the step as eager launches instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--component", choices=["decode", "block_manager", "block_copy"], default="decode",

@@ -359,18 +359,23 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     NR = std::min(NR, chunk_bound);
     p.NR = static_cast<int>(NR);
 
+    // Both launches are programmatic dependents of the work before them on
+    // the stream; each kernel waits (griddepcontrol.wait) for that work to
+    // complete before it reads anything, so only the launch overlaps.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(NR * NHG));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     void* args[] = {&p, &tk, &tv, &tq};
     ce = cudaLaunchKernelExC(&cfg, kern, args);
     if (ce != cudaSuccess) return fail_cuda("decode: main kernel launch", ce);
 
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg{};
     {
         // persistent reduce grid: one wave of CTAs striding over the

@@ -89,6 +89,9 @@ reshape_and_cache_kernel(uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
                          const uint8_t* __restrict__ key, const uint8_t* __restrict__ value,
                          const int64_t* __restrict__ slots, int T, int row_elems, int block_size,
                          int64_t nslots, float k_scale, float v_scale, int32_t* err) {
+    // a decode launched next may become resident now (it waits for this
+    // grid to complete before it reads anything)
+    grid_dependents_launch();
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -123,6 +126,7 @@ struct BlockCopyArgs {
 
 __global__ void __launch_bounds__(256)
 block_copy_kernel(const __grid_constant__ BlockCopyArgs a) {
+    grid_dependents_launch();
     const int p = blockIdx.x, l = blockIdx.y, kv = blockIdx.z;
     const int64_t src = a.pairs[2 * static_cast<int64_t>(p)], dst = a.pairs[2 * static_cast<int64_t>(p) + 1];
     if (src < 0 || src >= a.src_blocks || dst < 0 || dst >= a.dst_blocks) {

@@ -1578,9 +1578,14 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     int2* s_tot = reinterpret_cast<int2*>(s_first + 1);
     int* s_end = reinterpret_cast<int*>(s_tot + 1);
 
-    // The merge kernel is launched as a programmatic dependent of this one
-    // and waits (griddepcontrol.wait) for this grid to complete: letting it
-    // become resident now takes its launch off the critical path.
+    // This kernel is launched as a programmatic dependent of the previous
+    // kernel on the stream (typically the cache write): its CTAs may be
+    // resident before that grid ends, and wait here until it has completed
+    // and its writes are visible.  The merge kernel is in turn launched as a
+    // programmatic dependent of this one and waits for this grid to
+    // complete: letting it become resident now takes its launch off the
+    // critical path.
+    grid_dependency_wait();
     grid_dependents_launch();
     const int hg = blockIdx.x % p.NHG;
     const int range = blockIdx.x / p.NHG;
