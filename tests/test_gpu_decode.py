@@ -235,6 +235,32 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == 3
 
 
+def test_one_workspace_serves_calls_of_other_shapes():
+    """The workspace holds no state between calls: one buffer, filled with
+    garbage first, serves decode calls of different shapes in turn."""
+    wa = _case("f16", None, 128, 16, 28, 4, [3000, 17, 900, 5000, 64], seed=51)
+    wb = _case("bf16", None, 128, 16, 32, 8, [40, 7000, 1200], seed=52)
+
+    def need(wl):
+        return pa.pa_decode_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                           wl.block_tables.shape[1] * wl.block_size, 0)
+
+    ws = torch.full((max(need(wa), need(wb)),), 0x7f, dtype=torch.uint8, device="cuda")
+    steps, refs = {}, {}
+    for wl in (wa, wb):
+        ref_k, ref_v = oracle_caches(wl)
+        refs[wl.name] = oracle.decode(oracle_problem(wl, ref_k, ref_v))
+        steps[wl.name] = GpuStep(wl)
+        steps[wl.name].setup()
+        steps[wl.name].write_step()
+    for wl in (wa, wb, wa, wb):
+        step = steps[wl.name]
+        out = step.decode(workspace=ws)
+        torch.cuda.synchronize()
+        assert step.err.item() == 0
+        compare(out, refs[wl.name], wl.kv_dtype, wl.name)
+
+
 def test_needle_outputs_are_order_one():
     """Peaked attention (planted keys c*q/|q|): outputs are O(1), so the
     tolerance bites at long context."""
