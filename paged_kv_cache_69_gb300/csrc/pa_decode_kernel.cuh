@@ -262,9 +262,11 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
             const int L = clamp_len(p.seq_lens[i], maxL);
             const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
             if (L == 0) {
+                // no keys: zero outputs for every query row of the sequence
+                const int qa = p.q_start ? p.q_start[i] : i, qb = p.q_start ? p.q_start[i + 1] : i + 1;
                 uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                                    static_cast<size_t>(i) * p.Hq * p.D * p.out_bytes);
-                for (int k = 0; k < p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
+                                                    static_cast<size_t>(qa) * p.Hq * p.D * p.out_bytes);
+                for (int k = 0; k < (qb - qa) * p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
             } else {
                 const int r0 = range_of_pos(chunk_pos(p, S, U), W, p.NR);
                 const int r1 = range_of_pos(chunk_pos(p, S + nch - 1, U + nu - 1), W, p.NR);

@@ -65,6 +65,33 @@ def test_attention_matches_oracle(case):
     compare(out, ref, wl.kv_dtype, wl.name)
 
 
+def test_sequences_without_keys_or_with_fewer_keys_than_queries():
+    """A sequence with no keys gives zero rows for all its query tokens (and
+    leaves the other sequences' rows alone); with fewer keys than query
+    tokens, the tokens before the first key give zeros, as in the oracle."""
+    nq = [2, 3, 1, 3, 2]
+    wl, q, qs = _case("bf16", None, 128, 16, 32, 8, [5, 300, 9, 2, 50], nq, seed=81)
+    sl = wl.seq_lens.clone()
+    sl[0] = 0
+    sl[2] = 0
+    ref_k, ref_v = oracle_caches(wl)
+    ref = oracle.attention_causal(q, oracle.DTYPE_CODES[wl.q_dtype], ref_k, ref_v, oracle.DTYPE_CODES[wl.kv_dtype],
+                                  wl.block_tables, sl, qs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                  wl.block_size, wl.num_blocks, wl.scale)
+    step = GpuStep(wl)
+    step.setup()
+    step.write_step()
+    d = step.dev
+    out = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+    pa.pa_attention(out, q.cuda(), d.k_cache, d.v_cache, d.block_tables, sl.cuda(), qs.cuda(), d.scale, max(nq),
+                    err_flag=step.err)
+    torch.cuda.synchronize()
+    assert step.err.item() == 0
+    for i in (0, 2):
+        assert torch.count_nonzero(out[int(qs[i]):int(qs[i + 1])]) == 0
+    compare(out, ref, wl.kv_dtype, "no keys")
+
+
 @pytest.mark.parametrize("pt", [0, 512])
 def test_long_sequence_split_over_every_cta(pt):
     """One 40,000-token sequence with 8 query tokens: the merge combines the

@@ -261,6 +261,42 @@ def test_one_workspace_serves_calls_of_other_shapes():
         compare(out, refs[wl.name], wl.kv_dtype, wl.name)
 
 
+def test_graph_replay_of_write_and_decode_matches_eager():
+    """The cache write and the decode (main kernel + merge, each launched as a
+    programmatic dependent of the work before it) captured once as a CUDA
+    graph and replayed give the eager call's result bit for bit."""
+    wl = _case("bf16", None, 128, 16, 32, 8, [900, 17, 4000, 300], seed=61)
+    ref_k, ref_v = oracle_caches(wl)
+    ref = oracle.decode(oracle_problem(wl, ref_k, ref_v))
+    step = GpuStep(wl)
+    step.setup()
+    step.write_step()
+    d = step.dev
+    MB = d.block_tables.shape[1]
+    ws = pa.alloc_workspace(d.num_seqs, d.num_q_heads, d.head_dim, MB * d.block_size)
+    eager = torch.empty_like(d.q)
+    pa.pa_decode(eager, d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.scale, workspace=ws,
+                 err_flag=step.err)
+    torch.cuda.synchronize()
+    out = torch.full_like(d.q, float("nan"))
+
+    def one_step():
+        step.write_step()          # rewrites the same slots with the same values
+        pa.pa_decode(out, d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.scale, workspace=ws,
+                     err_flag=step.err)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        one_step()
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert step.err.item() == 0
+        assert torch.equal(out, eager)
+    compare(out, ref, wl.kv_dtype, wl.name)
+
+
 def test_needle_outputs_are_order_one():
     """Peaked attention (planted keys c*q/|q|): outputs are O(1), so the
     tolerance bites at long context."""
