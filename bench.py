@@ -109,6 +109,22 @@ def profile_traffic(workload: str):
 # ---------------------------------------------------------------------------
 # clocks during the timed region (NVML read-only queries)
 # ---------------------------------------------------------------------------
+def max_over_ranks(values, device, world):
+    """Each value's maximum over all ranks: the slowest rank sets the job's
+    time.  One all-reduce of a float64 vector (NCCL on GPUs, gloo on CPUs)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(units_per_rank_step, world, steps, ms_total):
+    """Units all ranks processed per second over the max-over-ranks time."""
+    return units_per_rank_step * world * steps / (ms_total / 1e3)
+
+
 def capture_graph(fn):
     """fn's launches captured as one CUDA graph, or None (with a note on
     stderr) when capture fails; the eager launches are then timed instead."""
@@ -380,10 +396,7 @@ def run_ours(args, rank, world, local) -> dict | None:
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     write_us = statistics.mean(a.elapsed_time(b) for a, b in ew) * 1e3
     copy_us = statistics.mean(a.elapsed_time(b) for a, b in ec) * 1e3 if pairs is not None else None
-    t = torch.tensor([ms_total, dec_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total, dec_ms = float(t[0]), float(t[1])
+    ms_total, dec_ms = max_over_ranks([ms_total, dec_ms], device, world)
     if err.item() != 0:
         raise RuntimeError(f"device error flag {err.item()} during the benchmark")
 
@@ -420,10 +433,8 @@ def run_ours(args, rank, world, local) -> dict | None:
             run_e2e()
         b.record(stream)
         torch.cuda.synchronize()
-        te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device=device)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": wl.num_seqs * world * K / (float(te[0]) / 1e3), "unit": "tokens/s",
+        (te,) = max_over_ranks([a.elapsed_time(b)], device, world)
+        e2e = {"value": job_throughput(wl.num_seqs, world, K, te), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:
@@ -439,7 +450,7 @@ def run_ours(args, rank, world, local) -> dict | None:
                wl.num_seqs * wl.num_q_heads * wl.head_dim * 2 * sizing.ELEM_BYTES[wl.q_dtype])
     peak, peak_src = measured_peak()
     achieved = alg / (dec_ms / 1e3) / 1e9
-    value = wl.num_seqs * NQ * world * K / (ms_total / 1e3)
+    value = job_throughput(wl.num_seqs * NQ, world, K, ms_total)
     res = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
            "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": wl.kv_dtype, "data": "synthetic",
