@@ -74,6 +74,9 @@ typedef enum {
 #define PA_ERRBIT_BAD_PAIR      4u   /* copy pair id outside [0, num_blocks) */
 #define PA_ERRBIT_SEQ_TOO_LONG  8u   /* seq_lens[i] < 0 or > max_blocks_per_seq*block_size */
 #define PA_ERRBIT_WAIT_TIMEOUT 16u   /* an internal pipeline wait exceeded its time limit */
+#define PA_ERRBIT_BAD_QUERY    32u   /* pa_attention: q_start entries not increasing within
+                                        [0, total_q], or a sequence with more than max_q_len
+                                        query tokens; its rows are left unwritten */
 
 /* Human-readable name of a status. */
 const char* pa_status_string(pa_status s);

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(HERE, "libpa.so")
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = 0, 1, 2, 3, 4
 PA_OK = 0
 ERRBIT_BAD_BLOCK, ERRBIT_BAD_SLOT, ERRBIT_BAD_PAIR, ERRBIT_SEQ_TOO_LONG, ERRBIT_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+ERRBIT_BAD_QUERY = 32
 
 # entry points declared in include/pa.h
 EXPORTED = ("pa_status_string", "pa_last_error_detail", "pa_decode_workspace_size", "pa_decode",

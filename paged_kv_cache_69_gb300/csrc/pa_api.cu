@@ -235,6 +235,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.PC = partition_tokens / CT;
     p.q_start = q_start;
     p.QL = QL;
+    p.total_q = mq ? total_q : B;
     // Schedule weights: a unit start (query rows loaded, result written)
     // is charged 3/4 of a chunk, which balanced CTA finish times best on
     // length mixes with many short sequences.

@@ -76,6 +76,7 @@ struct DecodeParams {
     int PC;                   // partition length in chunks, 0 = none
     const int32_t* q_start;   // several query tokens per sequence: [B+1] row offsets; null = one each
     int QL;                   // most query tokens of a sequence (1 for decode)
+    int total_q;              // query rows in q / out
     int WQ, WS;               // schedule weights of a chunk and of a unit start
     int max_slots;
     float qk_scale;           // scale * log2(e) (* k_scale for fp8)
@@ -103,6 +104,18 @@ __device__ __forceinline__ int n_units(int L, int PC, int ct) {
     const int nch = cdiv_i(L, ct);
     return nch == 0 ? 0 : (PC > 0 ? cdiv_i(nch, PC) : 1);
 }
+// Query rows [qa, qa + qn) of sequence i: row i in decode, q_start[i] ..
+// q_start[i+1] with several query tokens.  Entries that are not increasing
+// inside [0, total_q], or give more than QL tokens, make the sequence's query
+// count 0 (nothing is read or written for it) and return false.
+__device__ __forceinline__ bool query_rows(const DecodeParams& p, int i, int& qa, int& qn) {
+    if (!p.q_start) { qa = i; qn = 1; return true; }
+    const int a = __ldg(p.q_start + i), b = __ldg(p.q_start + i + 1);
+    if (a < 0 || b < a || b > p.total_q || b - a > p.QL) { qa = 0; qn = 0; return false; }
+    qa = a; qn = b - a;
+    return true;
+}
+
 // Cost-weighted chunk stream.  Chunk k (global index) of global unit gu sits
 // at position WQ*k + WS*(gu + 1): each chunk weighs WQ and each unit start WS
 // more, for the per-segment work (query rows in, result out).  With
@@ -263,10 +276,11 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
             const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
             if (L == 0) {
                 // no keys: zero outputs for every query row of the sequence
-                const int qa = p.q_start ? p.q_start[i] : i, qb = p.q_start ? p.q_start[i + 1] : i + 1;
+                int qa, qn;
+                query_rows(p, i, qa, qn);
                 uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
                                                     static_cast<size_t>(qa) * p.Hq * p.D * p.out_bytes);
-                for (int k = 0; k < (qb - qa) * p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < qn * p.Hq * p.D * p.out_bytes / 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
             } else {
                 const int r0 = range_of_pos(chunk_pos(p, S, U), W, p.NR);
                 const int r1 = range_of_pos(chunk_pos(p, S + nch - 1, U + nu - 1), W, p.NR);
@@ -379,10 +393,11 @@ struct DecodeKernel {
         int qrow_i = i, qn_i = 1;
         auto load_q_rows = [&]() {
             if constexpr (MQ) {
-                const int a = i < p.B ? __ldg(p.q_start + i) : 0;
-                const int b = i < p.B ? __ldg(p.q_start + i + 1) : 0;
-                qrow_i = a;
-                qn_i = b - a;
+                if (i < p.B) {
+                    if (!query_rows(p, i, qrow_i, qn_i) && lane == 0) raise_flag(p.err_flag, PA_ERRBIT_BAD_QUERY);
+                } else {
+                    qrow_i = 0; qn_i = 0;
+                }
             } else {
                 qrow_i = i;
             }
@@ -1684,8 +1699,9 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
         if (WPI == 1 && h >= p.Hq) continue;
         int qrow = e.x;                                   // row of (sequence, token) in q / out
         if (p.q_start) {
-            const int a = p.q_start[e.x];
-            if (jq >= p.q_start[e.x + 1] - a) continue;   // the sequence has fewer query tokens
+            int a, qn;
+            query_rows(p, e.x, a, qn);
+            if (jq >= qn) continue;                       // the sequence has fewer query tokens
             qrow = a + jq;
         }
         // partial rows of this (token, head): slot * QL * Hq + jq * Hq + h

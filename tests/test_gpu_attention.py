@@ -92,6 +92,29 @@ def test_sequences_without_keys_or_with_fewer_keys_than_queries():
     compare(out, ref, wl.kv_dtype, "no keys")
 
 
+def test_malformed_query_offsets_are_flagged_and_skipped():
+    """q_start giving one sequence more than max_q_len tokens: that sequence
+    is skipped with ERRBIT_BAD_QUERY and the others are still right."""
+    nq = [2, 7, 2]
+    wl, q, qs = _case("bf16", None, 128, 16, 32, 8, [40, 300, 90], nq, seed=83)
+    ref_k, ref_v = oracle_caches(wl)
+    ref = oracle.attention_causal(q, oracle.DTYPE_CODES[wl.q_dtype], ref_k, ref_v, oracle.DTYPE_CODES[wl.kv_dtype],
+                                  wl.block_tables, wl.seq_lens, qs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                  wl.block_size, wl.num_blocks, wl.scale)
+    step = GpuStep(wl)
+    step.setup()
+    step.write_step()
+    d = step.dev
+    out = torch.zeros(q.shape, dtype=q.dtype, device="cuda")
+    pa.pa_attention(out, q.cuda(), d.k_cache, d.v_cache, d.block_tables, d.seq_lens, qs.cuda(), d.scale, 4,
+                    err_flag=step.err)
+    torch.cuda.synchronize()
+    assert step.err.item() & pa.ERRBIT_BAD_QUERY
+    keep = torch.cat([torch.arange(0, 2), torch.arange(9, 11)])
+    compare(out[keep], ref[keep.numpy()], wl.kv_dtype, "valid sequences")
+    assert torch.count_nonzero(out[2:9]) == 0      # the skipped sequence's rows are untouched
+
+
 @pytest.mark.parametrize("pt", [0, 512])
 def test_long_sequence_split_over_every_cta(pt):
     """One 40,000-token sequence with 8 query tokens: the merge combines the
