@@ -122,6 +122,38 @@ typedef struct {
 pa_bm_status pa_bm_block_tables_update(const pa_bm* m, int32_t n, const int64_t* reqs, int32_t* out,
                                        int32_t max_blocks, int32_t pad, pa_bm_row* rows);
 
+/*
+ * Preemption by swapping: a preempted request's KV is copied to CPU memory
+ * and its progress kept ("显存与 KV 缓存", section on preemption, 抢占;
+ * "vLLM intro part 2", section 9 weighs it against recomputation).  A
+ * second pool of host blocks 0..num_host_blocks-1 receives the blocks; the
+ * pairs returned are the copies to make with pa_swap_blocks, on the stream,
+ * before anything else writes the blocks named as destinations.
+ *
+ * pa_bm_set_host_pool: (re)creates the host pool, free queue in `order`
+ * (nullable: 0, 1, 2, ...).  PA_BM_BAD_REQUEST while a request is swapped
+ * out.
+ */
+pa_bm_status pa_bm_set_host_pool(pa_bm* m, int32_t num_host_blocks, const int32_t* order);
+int32_t pa_bm_num_host_free(const pa_bm* m);
+
+/* Swap a complete request out: every block it holds alone (ref_cnt 1) gets
+ * a host block from the head of the host queue, in table order, and the
+ * pairs (gpu block, host block) go to pairs[2*p], pairs[2*p+1]; those GPU
+ * blocks are then released last block first, as by pa_bm_free.  Blocks it
+ * shares with other requests stay on the GPU with its reference (moving one
+ * holder would free no memory).  The request keeps its token count; until
+ * pa_bm_swap_in it has no block table and cannot append or fork.
+ * PA_BM_NO_SPACE (nothing changed) if the host queue is short. */
+pa_bm_status pa_bm_swap_out(pa_bm* m, int64_t req, int64_t* pairs, int32_t pair_cap, int32_t* num_pairs);
+
+/* Swap it back in: each host-resident entry, in table order, takes a GPU
+ * block from the free queue; pairs (host block, gpu block); the host blocks
+ * return to the tail of the host queue; the request's prompt blocks are
+ * registered under their prefix hashes again.  PA_BM_NO_SPACE (nothing
+ * changed) if the GPU free queue is short. */
+pa_bm_status pa_bm_swap_in(pa_bm* m, int64_t req, int64_t* pairs, int32_t pair_cap, int32_t* num_pairs);
+
 #ifdef __cplusplus
 }
 #endif

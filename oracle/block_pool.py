@@ -28,6 +28,16 @@ order and names:
   ("vLLM intro part 2" section 5, steps 1-4).
 * A finished request hands its blocks to ``free_blocks`` last block first
   ("分页省的不是 KV 字节" T2; "vLLM intro part 2" section 6.3, free step 1).
+* Preemption by swapping: a preempted request's KV goes to CPU memory and
+  its progress is kept ("显存与 KV 缓存", the preemption section, 抢占;
+  "vLLM intro part 2" section 9 weighs it against recomputation).  The
+  pages leave the block-level rule open; read here as: the blocks the
+  request holds alone (ref_cnt 1) move, in table order, to host blocks taken
+  from a host free queue, and are then released like a finished request's
+  (last first); blocks it shares stay on the GPU, since moving one holder
+  frees nothing.  Swapping in takes GPU blocks from the free queue's head in
+  table order, returns the host blocks to the host queue's tail and
+  registers the prompt blocks under their hashes again.
 
 The hash input is serialised as: parent digest (32 bytes; 32 zero bytes for
 block 0), the block's token ids as little-endian uint32, then the UTF-8
@@ -156,6 +166,8 @@ class Request:
         self.num_tokens = 0
         self.need = 0                       # blocks the request's tokens take
         self.hashes: List[bytes] = []       # hashes of its full prompt blocks
+        self.host: Dict[int, int] = {}      # swapped out: table entry -> host block
+        self.swapped = False
 
 
 class BlockManager:
@@ -166,6 +178,7 @@ class BlockManager:
         self.block_size = block_size
         self.pool = BlockPool(num_blocks, order)
         self.reqs: Dict[int, Request] = {}
+        self.host_free: List[int] = []      # host blocks, index 0 = next to be handed out
 
     def allocate(self, req_id: int, num_tokens: int, hashes: Sequence[bytes] = ()) -> Tuple[int, bool]:
         """A new request of ``num_tokens`` tokens whose full blocks have
@@ -214,8 +227,8 @@ class BlockManager:
         if child in self.reqs:
             raise KeyError(f"request {child} exists")
         p = self.reqs[parent]
-        if not self.is_complete(parent):
-            raise RuntimeError("fork of a waiting request")
+        if p.swapped or not self.is_complete(parent):
+            raise RuntimeError("fork of a waiting or swapped-out request")
         c = Request()
         c.blocks = list(p.blocks)
         c.num_tokens = p.num_tokens
@@ -228,8 +241,8 @@ class BlockManager:
         """Slot of the request's next token and the copy pair, if any; slot
         None (and no change) if the pool is short."""
         r = self.reqs[req_id]
-        if len(r.blocks) != r.need:
-            raise RuntimeError("append to a waiting request")
+        if r.swapped or len(r.blocks) != r.need:
+            raise RuntimeError("append to a waiting or swapped-out request")
         bs = self.block_size
         j, off = divmod(r.num_tokens, bs)
         pair = None
@@ -255,10 +268,62 @@ class BlockManager:
 
     def free(self, req_id: int) -> None:
         r = self.reqs.pop(req_id)
-        self.pool.free_blocks(list(reversed(r.blocks)))
+        self.pool.free_blocks([b for b in reversed(r.blocks) if b is not None])
+        for j in sorted(r.host):
+            self.host_free.append(r.host[j])
 
     def block_table(self, req_id: int) -> List[int]:
-        return [b.block_id for b in self.reqs[req_id].blocks]
+        r = self.reqs[req_id]
+        if r.swapped:
+            raise RuntimeError("a swapped-out request has no block table")
+        return [b.block_id for b in r.blocks]
+
+    def set_host_pool(self, num_host_blocks: int, order: Optional[Sequence[int]] = None) -> None:
+        if any(r.swapped for r in self.reqs.values()):
+            raise RuntimeError("host pool changed while a request is swapped out")
+        self.host_free = list(range(num_host_blocks) if order is None else order)
+
+    def swap_out(self, req_id: int) -> Optional[List[Tuple[int, int]]]:
+        """(gpu block, host block) pairs, or None (nothing changed) when the
+        host pool is short."""
+        r = self.reqs[req_id]
+        if r.swapped or len(r.blocks) != r.need:
+            raise RuntimeError("swap out of a waiting or swapped-out request")
+        private = [j for j, b in enumerate(r.blocks) if b.ref_cnt == 1]
+        if len(private) > len(self.host_free):
+            return None
+        pairs = []
+        for j in private:
+            h = self.host_free.pop(0)
+            pairs.append((r.blocks[j].block_id, h))
+            r.host[j] = h
+        self.pool.free_blocks([r.blocks[j] for j in reversed(private)])
+        for j in private:
+            r.blocks[j] = None
+        r.swapped = True
+        return pairs
+
+    def swap_in(self, req_id: int) -> Optional[List[Tuple[int, int]]]:
+        """(host block, gpu block) pairs, or None (nothing changed) when the
+        GPU free queue is short."""
+        r = self.reqs[req_id]
+        if not r.swapped:
+            raise RuntimeError("swap in of a request that is not swapped out")
+        js = sorted(r.host)
+        if len(js) > self.pool.get_num_free_blocks():
+            return None
+        fresh = self.pool.get_new_blocks(len(js))
+        pairs = []
+        for j, b in zip(js, fresh):
+            pairs.append((r.host[j], b.block_id))
+            r.blocks[j] = b
+        for j in js:
+            self.host_free.append(r.host[j])
+            if j < len(r.hashes):
+                self.pool.cache_full_block(r.blocks[j], r.hashes[j])
+        r.host = {}
+        r.swapped = False
+        return pairs
 
     def free_queue(self) -> List[Tuple[int, bool]]:
         return [(b.block_id, b.block_hash is not None) for b in self.pool.free_block_queue.items]

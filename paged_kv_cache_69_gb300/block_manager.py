@@ -28,7 +28,8 @@ HASH_BYTES = 32
 EXPORTED = ("pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_ref_cnt", "pa_bm_free_queue",
             "pa_bm_allocate", "pa_bm_resume", "pa_bm_fork", "pa_bm_append_slots", "pa_bm_cache_block",
             "pa_bm_free", "pa_bm_num_tokens", "pa_bm_block_table", "pa_bm_block_tables",
-            "pa_bm_block_tables_update")
+            "pa_bm_block_tables_update", "pa_bm_set_host_pool", "pa_bm_num_host_free", "pa_bm_swap_out",
+            "pa_bm_swap_in")
 ROW_DTYPE = np.dtype([("req", "<i8"), ("epoch", "<u4"), ("len", "<i4")])
 
 _lib = None
@@ -73,6 +74,13 @@ def host_lib():
         L.pa_bm_block_tables.argtypes = [vp, i32, vp, vp, i32, i32]
         L.pa_bm_block_tables_update.restype = ctypes.c_int
         L.pa_bm_block_tables_update.argtypes = [vp, i32, vp, vp, i32, i32, vp]
+        L.pa_bm_set_host_pool.restype = ctypes.c_int
+        L.pa_bm_set_host_pool.argtypes = [vp, i32, vp]
+        L.pa_bm_num_host_free.restype = i32
+        L.pa_bm_num_host_free.argtypes = [vp]
+        for name in ("pa_bm_swap_out", "pa_bm_swap_in"):
+            getattr(L, name).restype = ctypes.c_int
+            getattr(L, name).argtypes = [vp, i64, vp, i32, vp]
         _lib = L
     return _lib
 
@@ -192,6 +200,40 @@ class HostBlockManager:
         st = self.lib.pa_bm_free(self._h, int(req))
         if st != BM_OK:
             raise BlockManagerError(st, f"free request {req}")
+
+    # -- preemption by swapping ------------------------------------------------
+    def set_host_pool(self, num_host_blocks: int, order: Optional[Sequence[int]] = None) -> None:
+        o = None
+        if order is not None:
+            o = np.ascontiguousarray(np.asarray(order, dtype=np.int32))
+        st = self.lib.pa_bm_set_host_pool(self._h, int(num_host_blocks), None if o is None else _ptr(o))
+        if st != BM_OK:
+            raise BlockManagerError(st, "set_host_pool")
+
+    def num_host_free(self) -> int:
+        return int(self.lib.pa_bm_num_host_free(self._h))
+
+    def _swap(self, fn, req: int, what: str) -> Optional[np.ndarray]:
+        n = max(self.lib.pa_bm_block_table(self._h, int(req), None, 0), 0)
+        cap = max(n, self.num_blocks, 1)
+        pairs = np.empty((cap, 2), np.int64)
+        npairs = ctypes.c_int32(0)
+        st = fn(self._h, int(req), _ptr(pairs), cap, ctypes.byref(npairs))
+        if st == BM_NO_SPACE:
+            return None
+        if st != BM_OK:
+            raise BlockManagerError(st, f"{what} request {req}")
+        return pairs[:npairs.value].copy()
+
+    def swap_out(self, req: int) -> Optional[np.ndarray]:
+        """(gpu block, host block) pairs [p, 2] of the blocks the request
+        holds alone, or None (nothing changed) if the host pool is short."""
+        return self._swap(self.lib.pa_bm_swap_out, req, "swap out")
+
+    def swap_in(self, req: int) -> Optional[np.ndarray]:
+        """(host block, gpu block) pairs [p, 2], or None (nothing changed)
+        if the GPU free queue is short."""
+        return self._swap(self.lib.pa_bm_swap_in, req, "swap in")
 
     def num_tokens(self, req: int) -> int:
         return int(self.lib.pa_bm_num_tokens(self._h, int(req)))

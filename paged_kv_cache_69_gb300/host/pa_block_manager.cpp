@@ -9,6 +9,7 @@
 // under them, in registration order; a lookup takes the first.
 #include <cstdint>
 #include <cstring>
+#include <deque>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -35,6 +36,8 @@ struct Request {
     int64_t num_tokens = 0;
     int32_t need = 0;             // blocks its tokens take
     uint32_t epoch = 0;           // changes whenever an existing table entry changes
+    bool swapped = false;         // swapped out: host[j] >= 0 names the host block of entry j,
+    std::vector<int32_t> host;    // whose GPU entry blocks[j] is then -1
 };
 
 }  // namespace
@@ -48,6 +51,9 @@ struct pa_bm {
     std::unordered_map<Hash32, std::vector<int32_t>, Hash32Fn> cached;
     std::unordered_map<int64_t, Request> reqs;
     uint32_t next_epoch = 0;      // fresh epochs for new requests and copy-on-write
+    int32_t nh = 0;               // host blocks for swapping, 0 .. nh-1
+    std::deque<int32_t> host_free;   // free host blocks, head = next to be handed out
+    int32_t nswapped = 0;
 
     // ---- free queue ----
     void push_back(int32_t b) {
@@ -202,7 +208,7 @@ pa_bm_status pa_bm_fork(pa_bm* m, int64_t parent, int64_t child) {
     auto it = m->reqs.find(parent);
     if (it == m->reqs.end() || m->reqs.count(child)) return PA_BM_BAD_REQUEST;
     const Request& p = it->second;
-    if (static_cast<int32_t>(p.blocks.size()) != p.need) return PA_BM_BAD_REQUEST;
+    if (p.swapped || static_cast<int32_t>(p.blocks.size()) != p.need) return PA_BM_BAD_REQUEST;
     try {
         Request c;
         c.epoch = m->next_epoch++;
@@ -227,7 +233,7 @@ pa_bm_status pa_bm_append_slots(pa_bm* m, int32_t n, const int64_t* reqs, int64_
         auto it = m->reqs.find(reqs[k]);
         if (it == m->reqs.end()) { st = PA_BM_BAD_REQUEST; break; }
         Request& r = it->second;
-        if (static_cast<int32_t>(r.blocks.size()) != r.need) { st = PA_BM_BAD_REQUEST; break; }
+        if (r.swapped || static_cast<int32_t>(r.blocks.size()) != r.need) { st = PA_BM_BAD_REQUEST; break; }
         const int64_t j = r.num_tokens / m->bs;
         const int32_t off = static_cast<int32_t>(r.num_tokens % m->bs);
         if (off == 0) {
@@ -259,7 +265,7 @@ pa_bm_status pa_bm_append_slots(pa_bm* m, int32_t n, const int64_t* reqs, int64_
 pa_bm_status pa_bm_cache_block(pa_bm* m, int64_t req, int32_t j, const uint8_t* hash) {
     if (!m || !hash) return PA_BM_INVALID_ARG;
     auto it = m->reqs.find(req);
-    if (it == m->reqs.end()) return PA_BM_BAD_REQUEST;
+    if (it == m->reqs.end() || it->second.swapped) return PA_BM_BAD_REQUEST;
     if (j < 0 || j >= static_cast<int32_t>(it->second.blocks.size())) return PA_BM_INVALID_ARG;
     Hash32 h;
     std::memcpy(h.b, hash, PA_BM_HASH_BYTES);
@@ -276,7 +282,13 @@ pa_bm_status pa_bm_free(pa_bm* m, int64_t req) {
     auto it = m->reqs.find(req);
     if (it == m->reqs.end()) return PA_BM_BAD_REQUEST;
     const std::vector<int32_t>& bl = it->second.blocks;
-    for (size_t k = bl.size(); k-- > 0;) m->release(bl[k]);     // last block first
+    for (size_t k = bl.size(); k-- > 0;)                        // last block first
+        if (bl[k] >= 0) m->release(bl[k]);
+    if (it->second.swapped) {                                    // its host blocks, in table order
+        for (int32_t h : it->second.host)
+            if (h >= 0) m->host_free.push_back(h);
+        m->nswapped -= 1;
+    }
     m->reqs.erase(it);
     return PA_BM_OK;
 }
@@ -290,7 +302,7 @@ int64_t pa_bm_num_tokens(const pa_bm* m, int64_t req) {
 int32_t pa_bm_block_table(const pa_bm* m, int64_t req, int32_t* out, int32_t cap) {
     if (!m) return -1;
     auto it = m->reqs.find(req);
-    if (it == m->reqs.end()) return -1;
+    if (it == m->reqs.end() || it->second.swapped) return -1;
     const std::vector<int32_t>& bl = it->second.blocks;
     const int32_t n = static_cast<int32_t>(bl.size());
     for (int32_t k = 0; k < n && k < cap; ++k) out[k] = bl[static_cast<size_t>(k)];
@@ -302,7 +314,7 @@ pa_bm_status pa_bm_block_tables(const pa_bm* m, int32_t n, const int64_t* reqs, 
     if (!m || n < 0 || max_blocks < 0 || (n > 0 && (!reqs || !out))) return PA_BM_INVALID_ARG;
     for (int32_t k = 0; k < n; ++k) {
         auto it = m->reqs.find(reqs[k]);
-        if (it == m->reqs.end()) return PA_BM_BAD_REQUEST;
+        if (it == m->reqs.end() || it->second.swapped) return PA_BM_BAD_REQUEST;
         const std::vector<int32_t>& bl = it->second.blocks;
         if (static_cast<int64_t>(bl.size()) > max_blocks) return PA_BM_INVALID_ARG;
         int32_t* row = out + static_cast<size_t>(k) * max_blocks;
@@ -318,7 +330,7 @@ pa_bm_status pa_bm_block_tables_update(const pa_bm* m, int32_t n, const int64_t*
     if (!m || n < 0 || max_blocks < 0 || (n > 0 && (!reqs || !out || !rows))) return PA_BM_INVALID_ARG;
     for (int32_t k = 0; k < n; ++k) {
         auto it = m->reqs.find(reqs[k]);
-        if (it == m->reqs.end()) return PA_BM_BAD_REQUEST;
+        if (it == m->reqs.end() || it->second.swapped) return PA_BM_BAD_REQUEST;
         const Request& r = it->second;
         const int32_t len = static_cast<int32_t>(r.blocks.size());
         if (len > max_blocks) return PA_BM_INVALID_ARG;
@@ -335,6 +347,103 @@ pa_bm_status pa_bm_block_tables_update(const pa_bm* m, int32_t n, const int64_t*
         st.epoch = r.epoch;
         st.len = len;
     }
+    return PA_BM_OK;
+}
+
+pa_bm_status pa_bm_set_host_pool(pa_bm* m, int32_t num_host_blocks, const int32_t* order) {
+    if (!m || num_host_blocks < 0) return PA_BM_INVALID_ARG;
+    if (m->nswapped > 0) return PA_BM_BAD_REQUEST;
+    try {
+        std::vector<uint8_t> seen(static_cast<size_t>(num_host_blocks), 0);
+        std::deque<int32_t> q;
+        for (int32_t k = 0; k < num_host_blocks; ++k) {
+            const int32_t h = order ? order[k] : k;
+            if (h < 0 || h >= num_host_blocks || seen[static_cast<size_t>(h)]) return PA_BM_INVALID_ARG;
+            seen[static_cast<size_t>(h)] = 1;
+            q.push_back(h);
+        }
+        m->host_free.swap(q);
+        m->nh = num_host_blocks;
+    } catch (...) {
+        return PA_BM_INVALID_ARG;
+    }
+    return PA_BM_OK;
+}
+
+int32_t pa_bm_num_host_free(const pa_bm* m) { return m ? static_cast<int32_t>(m->host_free.size()) : -1; }
+
+pa_bm_status pa_bm_swap_out(pa_bm* m, int64_t req, int64_t* pairs, int32_t pair_cap, int32_t* num_pairs) {
+    if (!m || pair_cap < 0 || (pair_cap > 0 && !pairs)) return PA_BM_INVALID_ARG;
+    auto it = m->reqs.find(req);
+    if (it == m->reqs.end()) return PA_BM_BAD_REQUEST;
+    Request& r = it->second;
+    if (r.swapped || static_cast<int32_t>(r.blocks.size()) != r.need) return PA_BM_BAD_REQUEST;
+    // blocks held by this request alone move; shared ones stay (moving one
+    // holder would not free their memory)
+    int32_t priv = 0;
+    for (int32_t b : r.blocks) priv += (m->ref[b] == 1) ? 1 : 0;
+    if (priv > static_cast<int32_t>(m->host_free.size())) return PA_BM_NO_SPACE;
+    if (priv > pair_cap) return PA_BM_INVALID_ARG;
+    try {
+        r.host.assign(r.blocks.size(), -1);
+    } catch (...) {
+        return PA_BM_INVALID_ARG;
+    }
+    int32_t np = 0;
+    for (size_t j = 0; j < r.blocks.size(); ++j) {
+        if (m->ref[r.blocks[j]] != 1) continue;
+        const int32_t h = m->host_free.front();
+        m->host_free.pop_front();
+        pairs[2 * np] = r.blocks[j];
+        pairs[2 * np + 1] = h;
+        ++np;
+        r.host[j] = h;
+    }
+    for (size_t j = r.blocks.size(); j-- > 0;) {              // released last block first
+        if (r.host[j] < 0) continue;
+        m->release(r.blocks[j]);
+        r.blocks[j] = -1;
+    }
+    r.swapped = true;
+    r.epoch = m->next_epoch++;
+    m->nswapped += 1;
+    if (num_pairs) *num_pairs = np;
+    return PA_BM_OK;
+}
+
+pa_bm_status pa_bm_swap_in(pa_bm* m, int64_t req, int64_t* pairs, int32_t pair_cap, int32_t* num_pairs) {
+    if (!m || pair_cap < 0 || (pair_cap > 0 && !pairs)) return PA_BM_INVALID_ARG;
+    auto it = m->reqs.find(req);
+    if (it == m->reqs.end()) return PA_BM_BAD_REQUEST;
+    Request& r = it->second;
+    if (!r.swapped) return PA_BM_BAD_REQUEST;
+    int32_t cnt = 0;
+    for (int32_t h : r.host) cnt += (h >= 0) ? 1 : 0;
+    if (cnt > m->nfree) return PA_BM_NO_SPACE;
+    if (cnt > pair_cap) return PA_BM_INVALID_ARG;
+    int32_t np = 0;
+    for (size_t j = 0; j < r.host.size(); ++j) {
+        if (r.host[j] < 0) continue;
+        const int32_t b = m->take();
+        pairs[2 * np] = r.host[j];
+        pairs[2 * np + 1] = b;
+        ++np;
+        r.blocks[j] = b;
+    }
+    try {
+        for (size_t j = 0; j < r.host.size(); ++j) {
+            if (r.host[j] < 0) continue;
+            m->host_free.push_back(r.host[j]);
+            if (j < r.hashes.size()) m->cache_block(r.blocks[j], r.hashes[j]);   // prompt blocks stay findable
+        }
+    } catch (...) {
+        return PA_BM_INVALID_ARG;
+    }
+    r.host.clear();
+    r.swapped = false;
+    r.epoch = m->next_epoch++;
+    m->nswapped -= 1;
+    if (num_pairs) *num_pairs = np;
     return PA_BM_OK;
 }
 

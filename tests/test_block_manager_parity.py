@@ -221,3 +221,119 @@ def test_incremental_block_tables_equal_full_tables():
         rnd.shuffle(live)
         got = buf.update(m, live)
         assert np.array_equal(got, m.block_tables(live, maxb, pad=-3)), f"step {step}"
+
+
+def _state_swap(m, live, swapped, nb):
+    q, tables, refs = _state(m, live, nb)
+    host_free = m.num_host_free() if isinstance(m, hbm.HostBlockManager) else len(m.host_free)
+    return q, tables, refs, host_free
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_traces_with_swapping_match_oracle(seed):
+    """Random traces with swap-out / swap-in of complete requests (pairs
+    compared), interleaved with allocations, forks (shared blocks stay on the
+    GPU when one holder is swapped out), appends with copy-on-write and
+    frees of resident and swapped-out requests."""
+    rnd = random.Random(2000 + seed)
+    bs = rnd.choice([4, 8])
+    nb = rnd.choice([24, 60])
+    nh = rnd.choice([6, 20, 50])
+    order = rnd.sample(range(nb), nb)
+    horder = rnd.sample(range(nh), nh)
+    ref = bp.BlockManager(nb, bs, order)
+    dut = hbm.HostBlockManager(nb, bs, order)
+    ref.set_host_pool(nh, horder)
+    dut.set_host_pool(nh, horder)
+    prompts = [_toks(rnd.randrange(1, 6 * bs), 11 * seed + i) for i in range(4)]
+    live, swapped, nxt = [], [], 0
+    for step in range(300):
+        op = rnd.random()
+        if op < 0.2 or not live:
+            p = rnd.choice(prompts)[:rnd.randrange(1, 6 * bs)]
+            hs = bp.chain_hashes(p, bs)
+            got = dut.allocate(nxt, len(p), hs)
+            assert got == ref.allocate(nxt, len(p), hs)
+            if got[1]:
+                live.append(nxt)
+            else:
+                dut.free(nxt)
+                ref.free(nxt)
+            nxt += 1
+        elif op < 0.3:
+            par = rnd.choice(live)
+            dut.fork(par, nxt)
+            ref.fork(par, nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.45:
+            r = rnd.choice(live)
+            got = dut.swap_out(r)
+            want = ref.swap_out(r)
+            assert (got is None) == (want is None), f"step {step}"
+            if got is not None:
+                assert got.tolist() == [list(x) for x in want], f"step {step}"
+                live.remove(r)
+                swapped.append(r)
+        elif op < 0.6 and swapped:
+            r = rnd.choice(swapped)
+            got = dut.swap_in(r)
+            want = ref.swap_in(r)
+            assert (got is None) == (want is None), f"step {step}"
+            if got is not None:
+                assert got.tolist() == [list(x) for x in want], f"step {step}"
+                swapped.remove(r)
+                live.append(r)
+        elif op < 0.85:
+            batch = rnd.sample(live, rnd.randrange(1, min(len(live), 5) + 1))
+            slots, pairs, done = dut.append_slots(batch)
+            want_slots, want_pairs = [], []
+            for r in batch:
+                s, pr = ref.append_slot(r)
+                if s is None:
+                    break
+                want_slots.append(s)
+                if pr is not None:
+                    want_pairs.append(list(pr))
+            assert done == len(want_slots)
+            assert slots[:done].tolist() == want_slots and pairs.tolist() == want_pairs
+        else:
+            pool = live + swapped
+            r = pool[rnd.randrange(len(pool))]
+            (live if r in live else swapped).remove(r)
+            dut.free(r)
+            ref.free(r)
+        assert _state_swap(dut, live, swapped, nb) == _state_swap(ref, live, swapped, nb), f"step {step}"
+
+
+def test_swap_out_keeps_shared_blocks_and_swap_in_restores_the_table_shape():
+    """A 3-block request forked once: after one more token each (the shared
+    partly filled last block is copied for the first), swapping out the
+    first moves only its private blocks; its prompt blocks, shared with the
+    fork, stay; swap-in gives fresh GPU blocks in table order and frees the
+    host blocks."""
+    bs, nb = 4, 12
+    m = hbm.HostBlockManager(nb, bs)
+    m.set_host_pool(4)
+    m.allocate(0, 10)                                  # blocks 0, 1, 2 (last holds 2 tokens)
+    m.fork(0, 1)
+    slots, pairs, done = m.append_slots([0])           # request 0 copies block 2 -> 3
+    assert pairs.tolist() == [[2, 3]] and m.block_table(0) == [0, 1, 3]
+    out = m.swap_out(0)
+    assert out.tolist() == [[3, 0]]                    # only its private block; host block 0
+    assert m.num_host_free() == 3 and m.ref_count(3) == 0 and m.ref_count(0) == 2
+    with pytest.raises(hbm.BlockManagerError):
+        m.append_slots([0])
+    with pytest.raises(hbm.BlockManagerError):
+        m.fork(0, 5)
+    with pytest.raises(hbm.BlockManagerError):
+        m.block_tables([0], 4)
+    assert m.block_table(1) == [0, 1, 2]               # the fork is untouched
+    back = m.swap_in(0)
+    assert back.tolist() == [[0, 3]]                   # block 3 was the free queue's head again
+    assert m.block_table(0) == [0, 1, 3] and m.num_host_free() == 4 and m.num_tokens(0) == 11
+    with pytest.raises(hbm.BlockManagerError):
+        m.swap_in(0)                                   # not swapped out
+    # a host pool too small: nothing changes
+    m.set_host_pool(0)
+    assert m.swap_out(0) is None and m.block_table(0) == [0, 1, 3]
