@@ -71,6 +71,9 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, pa_dtype q_dtyp
     if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
         static_cast<long long>(max_blocks_per_seq) * block_size >= (1LL << 30))
         return fail(PA_ERR_INVALID_ARG, "decode_noalloc: sizes must be positive");
+    int dev = 0;
+    const cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return fail_cuda("decode_noalloc: no current device", de);
     const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
                                                  max_blocks_per_seq * block_size, partition_tokens);
     if (need == 0) return fail(PA_ERR_INVALID_ARG, "decode_noalloc: invalid sizes for the scratch bound");

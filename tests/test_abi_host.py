@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_cache_69_gb300 as pa
 from paged_kv_cache_69_gb300 import build_lib as pabuild
@@ -105,3 +106,52 @@ def test_block_copy_host_validation(lib):
                               None, None) == 1
     assert lib.pa_swap_blocks(vp(16), vp(16), 0, vp(16), vp(16), 8, pa.PA_F16, vp(16), 1, 2, 128, 16,
                               None, None) == 1
+
+
+def _attention_args(**over):
+    a = dict(out=16, q=16, qd=pa.PA_F16, k=16, v=16, kvd=pa.PA_F16, bt=16, mb=4, sl=16, qs=16, B=2, TQ=4,
+             MQ=2, Hq=4, Hkv=2, D=128, bs=16, NB=8, scale=0.1, ks=1.0, vs=1.0, P=0, ws=256, wsb=1 << 20,
+             err=None, stream=None)
+    a.update(over)
+    return tuple(a[k] for k in ("out", "q", "qd", "k", "v", "kvd", "bt", "mb", "sl", "qs", "B", "TQ", "MQ",
+                                "Hq", "Hkv", "D", "bs", "NB", "scale", "ks", "vs", "P", "ws", "wsb", "err",
+                                "stream"))
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qs=None), 1),                         # no query offsets
+    (dict(MQ=0), 1),                            # max_q_len must be >= 1
+    (dict(TQ=-1), 1),                           # negative total
+    (dict(Hq=5), 1),                            # checks shared with decode
+    (dict(D=96), 2),
+    (dict(kvd=pa.PA_F32, qd=pa.PA_F32), 2),     # tensor cores only: no f32 cache
+])
+def test_attention_host_validation(lib, over, status):
+    assert lib.pa_attention(*_attention_args(**over)) == status
+    assert lib.pa_last_error_detail().decode() != ""
+
+
+def test_attention_without_query_tokens_is_a_noop(lib):
+    assert lib.pa_attention(*_attention_args(TQ=0)) == 0
+    assert lib.pa_attention(*_attention_args(B=0, TQ=0)) == 0
+
+
+def test_workspace_sizes_reject_bad_sizes(lib):
+    assert lib.pa_decode_workspace_size(-1, 4, 128, 100, 0) == 0
+    assert lib.pa_decode_workspace_size(2, 0, 128, 100, 0) == 0
+    assert lib.pa_attention_workspace_size(2, 0, 4, 128, 100, 0) == 0
+    assert lib.pa_attention_workspace_size(2, 2, 4, 128, -5, 0) == 0
+
+
+def test_noalloc_host_validation(lib):
+    args = list(_decode_args())
+    noalloc = args[:19] + args[21:]           # pa_decode's arguments without the workspace pair
+    if not torch.cuda.is_available():
+        assert lib.pa_decode_noalloc(*noalloc) == 4            # PA_ERR_CUDA: no device to size scratch on
+        assert "device" in lib.pa_last_error_detail().decode()
+    empty = list(noalloc)
+    empty[9] = 0                              # num_seqs = 0: nothing to do
+    assert lib.pa_decode_noalloc(*empty) == 0
+    bad = list(noalloc)
+    bad[10] = 0                               # num_q_heads = 0
+    assert lib.pa_decode_noalloc(*bad) == 1
