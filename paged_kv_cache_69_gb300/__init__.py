@@ -112,6 +112,8 @@ def _ptr(t: Optional[torch.Tensor]):
 def _code(t: torch.Tensor, override=None) -> int:
     if override is not None:
         return _NAME_CODE[override] if isinstance(override, str) else int(override)
+    if t.dtype not in _DTYPE_CODE:
+        raise ValueError(f"libpa has no element type for {t.dtype}")
     return _DTYPE_CODE[t.dtype]
 
 
@@ -127,6 +129,27 @@ def _dev(*ts):
             raise ValueError("libpa works on CUDA tensors only")
         if t is not None and not t.is_contiguous():
             raise ValueError("libpa expects contiguous tensors")
+
+
+def _pools(k: torch.Tensor, v: torch.Tensor):
+    """K and V pools of one shape and element type; returns (NB, bs, Hkv, D)."""
+    if k.dim() != 4 or tuple(v.shape) != tuple(k.shape) or v.dtype != k.dtype:
+        raise ValueError("k_cache and v_cache must be [num_blocks, block_size, num_kv_heads, head_dim] "
+                         "of one shape and dtype")
+    return tuple(k.shape)
+
+
+def _tables(block_tables: torch.Tensor, seq_lens: torch.Tensor, B: int):
+    """int32 block tables with a row per sequence and int32 seq_lens [B]."""
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] < B or seq_lens.numel() != B:
+        raise ValueError("block_tables must be [>= num_seqs, max_blocks] and seq_lens [num_seqs]")
+
+
+def _flag(err_flag: Optional[torch.Tensor]):
+    if err_flag is not None and (err_flag.dtype != torch.int32 or err_flag.numel() < 1):
+        raise ValueError("err_flag must be an int32 tensor of at least one element")
 
 
 # ---------------------------------------------------------------------------
@@ -154,11 +177,12 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
     dtype (uint8 storage means fp8-e4m3)."""
     _dev(out, q, k_cache, v_cache, block_tables, seq_lens, workspace, err_flag)
     B, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
-    if D2 != D or tuple(out.shape) != (B, Hq, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
-        raise ValueError("shape mismatch between q, out, k_cache and v_cache")
-    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise ValueError("block_tables and seq_lens must be int32")
+    NB, bs, Hkv, D2 = _pools(k_cache, v_cache)
+    if D2 != D or tuple(out.shape) != (B, Hq, D) or out.dtype != q.dtype:
+        raise ValueError("q and out must be [num_seqs, num_q_heads, head_dim] of one dtype, head_dim "
+                         "that of the pools")
+    _tables(block_tables, seq_lens, B)
+    _flag(err_flag)
     MB = block_tables.shape[1]
     if workspace is None:
         workspace = alloc_workspace(B, Hq, D, MB * bs, partition_tokens, device=q.device)
@@ -179,11 +203,12 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     (NOALLOC_SCRATCH_BYTES per GPU, shared by all calls on that GPU)."""
     _dev(out, q, k_cache, v_cache, block_tables, seq_lens, err_flag)
     B, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
-    if D2 != D or tuple(out.shape) != (B, Hq, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
-        raise ValueError("shape mismatch between q, out, k_cache and v_cache")
-    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise ValueError("block_tables and seq_lens must be int32")
+    NB, bs, Hkv, D2 = _pools(k_cache, v_cache)
+    if D2 != D or tuple(out.shape) != (B, Hq, D) or out.dtype != q.dtype:
+        raise ValueError("q and out must be [num_seqs, num_q_heads, head_dim] of one dtype, head_dim "
+                         "that of the pools")
+    _tables(block_tables, seq_lens, B)
+    _flag(err_flag)
     _check(lib().pa_decode_noalloc(_ptr(out), _ptr(q), _code(q), _ptr(k_cache), _ptr(v_cache),
                                    _code(k_cache, kv_dtype), _ptr(block_tables), block_tables.shape[1],
                                    _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, float(scale), float(k_scale),
@@ -197,10 +222,11 @@ def pa_reshape_and_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, key: torc
                          err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
     """Write key/value [T, Hkv, D] into pool slots slot_mapping (int64 [T])."""
     _dev(k_cache, v_cache, key, value, slot_mapping, err_flag)
-    NB, bs, Hkv, D = k_cache.shape
+    NB, bs, Hkv, D = _pools(k_cache, v_cache)
     T = key.shape[0]
-    if tuple(key.shape) != (T, Hkv, D) or tuple(value.shape) != (T, Hkv, D):
-        raise ValueError("key/value must be [num_tokens, num_kv_heads, head_dim]")
+    if tuple(key.shape) != (T, Hkv, D) or tuple(value.shape) != (T, Hkv, D) or value.dtype != key.dtype:
+        raise ValueError("key/value must be [num_tokens, num_kv_heads, head_dim] of one dtype")
+    _flag(err_flag)
     if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
         raise ValueError("slot_mapping must be int64 [num_tokens]")
     _check(lib().pa_reshape_and_cache(_ptr(k_cache), _ptr(v_cache), _code(k_cache, kv_dtype), _ptr(key),
@@ -212,7 +238,8 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: 
                    kv_dtype=None, *, err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
     """Copy whole blocks src -> dst for each row (src, dst) of block_mapping (int64 [P, 2])."""
     _dev(k_cache, v_cache, block_mapping, err_flag)
-    NB, bs, Hkv, D = k_cache.shape
+    NB, bs, Hkv, D = _pools(k_cache, v_cache)
+    _flag(err_flag)
     if block_mapping.dtype != torch.int64 or (block_mapping.numel() and block_mapping.shape[-1] != 2):
         raise ValueError("block_mapping must be int64 [num_pairs, 2]")
     P = block_mapping.numel() // 2
@@ -226,7 +253,8 @@ def pa_copy_blocks_layers(k_caches, v_caches, block_mapping: torch.Tensor, kv_dt
     if len(k_caches) != len(v_caches) or not k_caches:
         raise ValueError("k_caches and v_caches must be equal-length non-empty lists")
     _dev(*k_caches, *v_caches, block_mapping, err_flag)
-    NB, bs, Hkv, D = k_caches[0].shape
+    NB, bs, Hkv, D = _pools(k_caches[0], v_caches[0])
+    _flag(err_flag)
     for t in list(k_caches) + list(v_caches):
         if tuple(t.shape) != (NB, bs, Hkv, D) or t.dtype != k_caches[0].dtype:
             raise ValueError("all pools must have one shape and dtype")
@@ -251,10 +279,11 @@ def pa_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor
         if not (t.is_cuda or t.is_pinned()):
             raise ValueError("pools must be device memory or pinned host memory")
     _dev(block_mapping, err_flag)
-    NBd, bs, Hkv, D = dst_k.shape
-    NBs = src_k.shape[0]
-    if tuple(src_k.shape[1:]) != (bs, Hkv, D) or dst_v.shape != dst_k.shape or src_v.shape != src_k.shape:
-        raise ValueError("pools must share the block shape")
+    _flag(err_flag)
+    NBd, bs, Hkv, D = _pools(dst_k, dst_v)
+    NBs = _pools(src_k, src_v)[0]
+    if tuple(src_k.shape[1:]) != (bs, Hkv, D) or src_k.dtype != dst_k.dtype:
+        raise ValueError("pools must share the block shape and dtype")
     if block_mapping.dtype != torch.int64 or (block_mapping.numel() and block_mapping.shape[-1] != 2):
         raise ValueError("block_mapping must be int64 [num_pairs, 2]")
     _check(lib().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), NBd, _ptr(src_k), _ptr(src_v), NBs,
@@ -279,14 +308,15 @@ def pa_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
     seq_lens[i]; max_q_len bounds every sequence's query count."""
     _dev(out, q, k_cache, v_cache, block_tables, seq_lens, q_start, workspace, err_flag)
     T, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
-    B = seq_lens.shape[0]
-    if D2 != D or tuple(out.shape) != (T, Hq, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
-        raise ValueError("shape mismatch between q, out, k_cache and v_cache")
-    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32 or q_start.dtype != torch.int32:
-        raise ValueError("block_tables, seq_lens and q_start must be int32")
-    if q_start.numel() != B + 1:
-        raise ValueError("q_start must have num_seqs + 1 entries")
+    NB, bs, Hkv, D2 = _pools(k_cache, v_cache)
+    B = seq_lens.numel()
+    if D2 != D or tuple(out.shape) != (T, Hq, D) or out.dtype != q.dtype:
+        raise ValueError("q and out must be [total_q, num_q_heads, head_dim] of one dtype, head_dim "
+                         "that of the pools")
+    _tables(block_tables, seq_lens, B)
+    _flag(err_flag)
+    if q_start.dtype != torch.int32 or q_start.numel() != B + 1:
+        raise ValueError("q_start must be int32 with num_seqs + 1 entries")
     MB = block_tables.shape[1]
     if workspace is None:
         n = pa_attention_workspace_size(B, max_q_len, Hq, D, MB * bs, partition_tokens)
