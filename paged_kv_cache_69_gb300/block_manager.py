@@ -191,6 +191,8 @@ class HostBlockManager:
         return int(slots[0]), (tuple(int(x) for x in pairs[0]) if len(pairs) else None)
 
     def cache_block(self, req: int, j: int, h: bytes) -> None:
+        if len(h) != HASH_BYTES:
+            raise ValueError("h must be a 32-byte digest")
         hb = np.frombuffer(h, np.uint8)
         st = self.lib.pa_bm_cache_block(self._h, int(req), int(j), _ptr(hb))
         if st != BM_OK:
@@ -206,6 +208,8 @@ class HostBlockManager:
         o = None
         if order is not None:
             o = np.ascontiguousarray(np.asarray(order, dtype=np.int32))
+            if o.shape != (int(num_host_blocks),):
+                raise ValueError("order must list every host block once")
         st = self.lib.pa_bm_set_host_pool(self._h, int(num_host_blocks), None if o is None else _ptr(o))
         if st != BM_OK:
             raise BlockManagerError(st, "set_host_pool")
@@ -252,6 +256,9 @@ class HostBlockManager:
         r = np.ascontiguousarray(np.asarray(reqs, dtype=np.int64))
         if out is None:
             out = np.empty((max(r.shape[0], 1), max_blocks), np.int32)
+        elif (out.dtype != np.int32 or out.ndim != 2 or not out.flags.c_contiguous
+              or out.shape[0] < r.shape[0] or out.shape[1] != max_blocks):
+            raise ValueError("out must be a C-contiguous int32 array [>= len(reqs), max_blocks]")
         st = self.lib.pa_bm_block_tables(self._h, r.shape[0], _ptr(r), _ptr(out), int(max_blocks), int(pad))
         if st != BM_OK:
             raise BlockManagerError(st, "block_tables")

@@ -167,6 +167,17 @@ def test_block_tables_layout_and_errors():
         m2.append_slots([1])
     m2.free(1)
     assert m2.num_free() == 2
+    # buffers the C++ side would write or read past are refused in the binding
+    with pytest.raises(ValueError):
+        m.block_tables([5, 6], 4, out=np.zeros((1, 4), np.int32))
+    with pytest.raises(ValueError):
+        m.block_tables([5, 6], 4, out=np.zeros((2, 4), np.int64))
+    with pytest.raises(ValueError):
+        m.cache_block(5, 0, b"short")
+    with pytest.raises(ValueError):
+        m.set_host_pool(4, [0, 1, 2])
+    out = np.full((3, 4), 9, np.int32)
+    assert m.block_tables([6], 4, out=out).tolist() == [[12, -1, -1, -1]]
 
 
 def test_decode_step_inputs_feed_the_gpu_calls():
