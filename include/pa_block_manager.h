@@ -98,7 +98,8 @@ pa_bm_status pa_bm_free(pa_bm* m, int64_t req);
 
 /* Number of tokens of a request, -1 if unknown. */
 int64_t pa_bm_num_tokens(const pa_bm* m, int64_t req);
-/* A request's block table: writes min(cap, n) ids, returns n or -1. */
+/* A request's block table: writes min(cap, n) ids (none when out is NULL),
+ * returns n, or -1 for an unknown or swapped-out request. */
 int32_t pa_bm_block_table(const pa_bm* m, int64_t req, int32_t* out, int32_t cap);
 /* Block tables of n requests as int32 rows of max_blocks entries, the
  * unused tail of each row set to `pad`: the layout pa_decode reads.

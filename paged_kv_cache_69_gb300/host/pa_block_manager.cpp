@@ -305,6 +305,7 @@ int32_t pa_bm_block_table(const pa_bm* m, int64_t req, int32_t* out, int32_t cap
     if (it == m->reqs.end() || it->second.swapped) return -1;
     const std::vector<int32_t>& bl = it->second.blocks;
     const int32_t n = static_cast<int32_t>(bl.size());
+    if (!out) cap = 0;                                          // size query
     for (int32_t k = 0; k < n && k < cap; ++k) out[k] = bl[static_cast<size_t>(k)];
     return n;
 }
