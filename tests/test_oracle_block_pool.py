@@ -178,3 +178,119 @@ def test_random_traces_keep_invariants(seed):
             r = live.pop(rnd.randrange(len(live)))
             m.free(r)
         _check_invariants(m, nb)
+
+
+class _Memory:
+    """Contents of every device and host block slot, moved only by what the
+    oracle's plans say: prompt writes into freshly allocated blocks, one
+    write per appended token, copy-on-write pairs, swap-out and swap-in
+    pairs.  A request's tokens must read back through its block table after
+    any sequence of such plans."""
+
+    def __init__(self, nb, nh, bs):
+        self.bs = bs
+        self.gpu = [[None] * bs for _ in range(nb)]
+        self.host = [[None] * bs for _ in range(nh)]
+
+    def read(self, table, n):
+        return [self.gpu[table[t // self.bs]][t % self.bs] for t in range(n)]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plans_preserve_every_requests_tokens(seed):
+    """Random traces of allocations with prefix hits, forks, appends with
+    copy-on-write, swap-out / swap-in and frees, replayed on a model of the
+    pool's contents: every resident request reads back exactly its own
+    tokens, whatever other requests wrote into blocks it gave up while
+    swapped out ("kv-cache-memory-core", preemption by swapping; "vLLM intro
+    part 2" section 5, copy-on-write)."""
+    rnd = random.Random(300 + seed)
+    bs, nb, nh = rnd.choice([4, 8]), rnd.choice([24, 48]), rnd.choice([8, 30])
+    m = bp.BlockManager(nb, bs, rnd.sample(range(nb), nb))
+    m.set_host_pool(nh, rnd.sample(range(nh), nh))
+    mem = _Memory(nb, nh, bs)
+    prompts = [_toks(6 * bs, 900 + 7 * seed + i) for i in range(3)]
+    want, live, swapped, nxt, fresh = {}, [], [], 0, 10 ** 6
+    swaps = 0
+    for step in range(400):
+        op = rnd.random()
+        if op < 0.2 or not live:
+            p = rnd.choice(prompts)[:rnd.randrange(1, 6 * bs)]
+            cached, ok = m.allocate(nxt, len(p), bp.chain_hashes(p, bs))
+            if not ok:
+                m.free(nxt)
+            else:
+                table = m.block_table(nxt)
+                for t in range(cached, len(p)):          # prefill writes what the cache did not hold
+                    mem.gpu[table[t // bs]][t % bs] = p[t]
+                want[nxt] = list(p)
+                live.append(nxt)
+            nxt += 1
+        elif op < 0.3:
+            par = rnd.choice(live)
+            m.fork(par, nxt)
+            want[nxt] = list(want[par])
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.6:
+            r = rnd.choice(live)
+            slot, pair = m.append_slot(r)
+            if slot is not None:
+                if pair is not None:
+                    mem.gpu[pair[1]] = list(mem.gpu[pair[0]])
+                mem.gpu[slot // bs][slot % bs] = fresh
+                want[r].append(fresh)
+                fresh += 1
+        elif op < 0.72:
+            r = rnd.choice(live)
+            pairs = m.swap_out(r)
+            if pairs is not None:
+                for g, h in pairs:
+                    mem.host[h] = list(mem.gpu[g])
+                live.remove(r)
+                swapped.append(r)
+                swaps += 1
+        elif op < 0.85 and swapped:
+            r = rnd.choice(swapped)
+            pairs = m.swap_in(r)
+            if pairs is not None:
+                for h, g in pairs:
+                    mem.gpu[g] = list(mem.host[h])
+                swapped.remove(r)
+                live.append(r)
+        else:
+            pool = live + swapped
+            r = pool[rnd.randrange(len(pool))]
+            (live if r in live else swapped).remove(r)
+            m.free(r)
+            del want[r]
+        for r in live:
+            assert mem.read(m.block_table(r), len(want[r])) == want[r], f"seed {seed} step {step} request {r}"
+    assert swaps > 5
+
+
+def test_contents_model_catches_a_swap_in_that_skips_a_block():
+    """The check above fails if swap-in leaves one swapped block behind (a
+    planted mistake in the oracle's plan, on the CPU)."""
+    bs = 4
+    m = bp.BlockManager(8, bs)
+    m.set_host_pool(4)
+    mem = _Memory(8, 4, bs)
+    p = list(range(100, 110))
+    m.allocate(0, len(p), [])
+    t = m.block_table(0)
+    for i, x in enumerate(p):
+        mem.gpu[t[i // bs]][i % bs] = x
+    for g, h in m.swap_out(0):
+        mem.host[h] = list(mem.gpu[g])
+    m.allocate(1, 12, [])                                # takes and overwrites the freed blocks
+    for b in m.block_table(1):
+        mem.gpu[b] = [-1] * bs
+    pairs = m.swap_in(0)
+    assert len(pairs) == 3
+    for h, g in pairs[:-1]:                              # the planted mistake: the last pair dropped
+        mem.gpu[g] = list(mem.host[h])
+    assert mem.read(m.block_table(0), len(p)) != p
+    h, g = pairs[-1]
+    mem.gpu[g] = list(mem.host[h])
+    assert mem.read(m.block_table(0), len(p)) == p
