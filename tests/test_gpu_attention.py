@@ -53,6 +53,7 @@ MQ_CASES = [
     ("f16", None, 128, 16, 8, 8, [100, 40, 17], [16, 16, 3], 0),             # MHA: 16 tokens x 1 head
     ("f16", None, 128, 16, 64, 4, [80, 600], [8, 2], 0),                     # 128 rows: 8 tiles
     ("bf16", None, 128, 8, 32, 8, [7, 200, 999], [4, 8, 2], 64),             # bs 8: two boxes per chunk
+    ("f16", None, 128, 64, 28, 4, [10, 64, 65, 700], [3, 8, 1, 8], 0),      # bs 64: chunks inside a block
     ("fp8_e4m3", "bf16", 128, 32, 32, 8, [90, 3000], [3, 6], 0),
     ("fp8_e5m2", "f16", 128, 16, 28, 4, [50, 900], [2, 4], 0),
 ]
