@@ -348,3 +348,33 @@ def test_swap_out_keeps_shared_blocks_and_swap_in_restores_the_table_shape():
     # a host pool too small: nothing changes
     m.set_host_pool(0)
     assert m.swap_out(0) is None and m.block_table(0) == [0, 1, 3]
+
+
+@pytest.mark.parametrize("impl", ["oracle", "cpp"])
+def test_swap_edge_cases(impl):
+    """A request whose blocks are all shared swaps out with no pairs and
+    back in unchanged; a host pool that is too small refuses the swap and
+    changes nothing; freeing a swapped-out request returns its host blocks."""
+    bs, nb = 4, 16
+    m = bp.BlockManager(nb, bs) if impl == "oracle" else hbm.HostBlockManager(nb, bs)
+    m.set_host_pool(2)
+    host_free = (lambda: len(m.host_free)) if impl == "oracle" else m.num_host_free
+    refc = m.ref_cnt if impl == "oracle" else m.ref_count
+    m.allocate(0, 8)                                   # two full blocks
+    m.fork(0, 1)                                       # both shared
+    table = m.block_table(0)
+    out = m.swap_out(0)
+    assert len(out) == 0 and host_free() == 2 and all(refc(b) == 2 for b in table)
+    back = m.swap_in(0)
+    assert len(back) == 0 and m.block_table(0) == table
+    m.allocate(2, 12)                                  # three private blocks, two host blocks
+    t2 = m.block_table(2)
+    free_before = m.num_free() if impl == "cpp" else m.pool.get_num_free_blocks()
+    assert m.swap_out(2) is None                       # refused: nothing changed
+    assert m.block_table(2) == t2 and host_free() == 2
+    assert (m.num_free() if impl == "cpp" else m.pool.get_num_free_blocks()) == free_before
+    m.allocate(3, 6)                                   # two private blocks: fits the host pool
+    pairs = m.swap_out(3)
+    assert len(pairs) == 2 and host_free() == 0
+    m.free(3)
+    assert host_free() == 2
