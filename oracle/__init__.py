@@ -12,8 +12,11 @@ Parity status of each function (what pins it, see tests/test_oracle_*.py):
     values of the format definition.
   - e4m3 encoder: brute-force nearest-value search over the decoded code
     table with ties to even, saturation cases, and torch's float8 cast.
-  - gather / attend / decode: dense contiguous attention in numpy, L=1 and
-    q=0 closed forms, a planted-key limit, block-permutation and aliasing
+  - gather / attend / decode: dense contiguous attention in numpy (f32, f16
+    and bf16 pools; e4m3 and e5m2 pools widened by torch's float8 types and
+    multiplied by k_scale / v_scale that differ 85-fold, with swapped and
+    dropped scales planted to show the check catches them), L=1 and q=0
+    closed forms, a planted-key limit, block-permutation and aliasing
     invariants, brute force on tiny cases, and planted-mistake checks.
   - reshape_and_cache / copy_blocks: numpy fancy-indexing restatements and
     the copy-on-write worked example of "vLLM intro part 2", section 5.

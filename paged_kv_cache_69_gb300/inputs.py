@@ -19,7 +19,8 @@ Conventions of every workload:
     NaN bit patterns; table entries past ``cdiv(seq_len, block_size)`` hold
     out-of-range garbage (-1 or num_blocks + 7).  A correct kernel reads none
     of them.
-  * Q, K, V values are N(0, 1) in float32, then cast to the storage type.
+  * Q, K, V values are N(0, 1) in float32 (keys and values optionally times
+    a constant), then cast to the storage type.
   * fp8 pools start as NaN bytes and are filled by a quantise-on-write cache
     write of bfloat16 sources; the per-tensor scales are max|x| / 448 over all
     K (resp. V) values ever written, computed in float32.
@@ -114,8 +115,9 @@ def _nan_pool(shape, kv_dtype: str, device) -> torch.Tensor:
     return torch.full(shape, NAN_BITS[kv_dtype], dtype=torch.int16, device=device).view(dt)
 
 
-def _randn(gen, shape, dtype, device) -> torch.Tensor:
-    return torch.randn(shape, generator=gen, dtype=torch.float32, device=device).to(dtype)
+def _randn(gen, shape, dtype, device, mult: float = 1.0) -> torch.Tensor:
+    x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+    return (x if mult == 1.0 else x * mult).to(dtype)
 
 
 def _tables_from_order(lens_blocks: Sequence[int], order: torch.Tensor, num_blocks: int,
@@ -141,15 +143,15 @@ def token_slots(block_tables: torch.Tensor, i: int, start: int, stop: int, block
 
 
 def _fill_history(wl_pool_k, wl_pool_v, block_tables, lens_old, Hkv, D, bs, dtype, gen, device,
-                  src_dtype, write_direct: bool):
+                  src_dtype, write_direct: bool, k_mult: float = 1.0, v_mult: float = 1.0):
     """Values for positions [0, lens_old[i]) of every sequence.  For 16/32-bit
     pools they are scattered straight into the pool; for fp8 pools they are
     returned as a cache write to replay through the quantising write."""
     slots = torch.cat([token_slots(block_tables, i, 0, int(n), bs) for i, n in enumerate(lens_old)]) \
         if len(lens_old) else torch.zeros(0, dtype=torch.int64)
     T = int(slots.numel())
-    k = _randn(gen, (T, Hkv, D), STORAGE[src_dtype], device)
-    v = _randn(gen, (T, Hkv, D), STORAGE[src_dtype], device)
+    k = _randn(gen, (T, Hkv, D), STORAGE[src_dtype], device, k_mult)
+    v = _randn(gen, (T, Hkv, D), STORAGE[src_dtype], device, v_mult)
     if write_direct:
         s = slots.to(device)
         wl_pool_k.view(-1, Hkv, D)[s] = k
@@ -201,8 +203,11 @@ def make_random(seq_lens: Sequence[int], *, num_q_heads: int, num_kv_heads: int,
                 block_size: int, kv_dtype: str, q_dtype: Optional[str] = None,
                 num_blocks: Optional[int] = None, spare_blocks: int = 0, seed: int = 0,
                 max_blocks_per_seq: Optional[int] = None, name: str = "random",
-                needles: int = 0, needle_c: float = 16.0, gen_device="cpu") -> Workload:
-    """A decode step over ``seq_lens`` (lengths after the step's append)."""
+                needles: int = 0, needle_c: float = 16.0, gen_device="cpu",
+                k_mult: float = 1.0, v_mult: float = 1.0) -> Workload:
+    """A decode step over ``seq_lens`` (lengths after the step's append).
+    ``k_mult`` / ``v_mult`` scale the N(0, 1) keys / values (an fp8 pool's
+    per-tensor scales then differ by their ratio)."""
     seq_lens = [int(x) for x in seq_lens]
     if any(L < 1 for L in seq_lens):
         raise ValueError("every sequence attends over at least its own new token")
@@ -227,9 +232,9 @@ def make_random(seq_lens: Sequence[int], *, num_q_heads: int, num_kv_heads: int,
     lens_old = [L - 1 for L in seq_lens]
     q = _randn(gen, (B, Hq, D), STORAGE[q_dtype], dev)
     hist = _fill_history(k_cache, v_cache, bt, lens_old, Hkv, D, bs, kv_dtype, gen, dev,
-                         src_dtype, write_direct=(kv_dtype not in FP8_MAX))
-    new_key = _randn(gen, (B, Hkv, D), STORAGE[src_dtype], dev)
-    new_value = _randn(gen, (B, Hkv, D), STORAGE[src_dtype], dev)
+                         src_dtype, write_direct=(kv_dtype not in FP8_MAX), k_mult=k_mult, v_mult=v_mult)
+    new_key = _randn(gen, (B, Hkv, D), STORAGE[src_dtype], dev, k_mult)
+    new_value = _randn(gen, (B, Hkv, D), STORAGE[src_dtype], dev, v_mult)
     slot_mapping = torch.cat([token_slots(bt, i, L - 1, L, bs) for i, L in enumerate(seq_lens)]) \
         if B else torch.zeros(0, dtype=torch.int64)
     wl = Workload(name=name, seed=seed, num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv,

@@ -4,6 +4,8 @@ produced by the GPU side."""
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -44,6 +46,24 @@ def oracle_problem(wl: inputs.Workload, k, v, block_tables=None, seq_lens=None) 
                           wl.seq_lens if seq_lens is None else seq_lens,
                           wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, wl.num_blocks,
                           wl.scale, wl.k_scale, wl.v_scale)
+
+
+def oracle_decode_threaded(prob: oracle.Problem, threads: int = 0) -> np.ndarray:
+    """oracle.decode's result, computed as one oracle.attend_one call per
+    (sequence, head) spread over host threads.  The oracle itself stays
+    single-threaded; its C calls release the GIL, so independent calls run
+    side by side.  Longest sequences go first so the threads finish together."""
+    out = np.zeros((prob.num_seqs, prob.num_q_heads, prob.head_dim), dtype=np.float64)
+    lens = prob.seq_lens.astype(np.int64)
+    pairs = sorted(((i, h) for i in range(prob.num_seqs) for h in range(prob.num_q_heads)),
+                   key=lambda ih: -int(lens[ih[0]]))
+
+    def one(ih):
+        out[ih[0], ih[1]] = oracle.attend_one(prob, ih[0], ih[1])
+
+    with ThreadPoolExecutor(max_workers=threads or max(1, min(32, os.cpu_count() or 1))) as ex:
+        list(ex.map(one, pairs))
+    return out
 
 
 class GpuStep:

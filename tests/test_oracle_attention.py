@@ -291,3 +291,103 @@ def test_zero_length_gives_zeros():
                                        1, 8, 8, wl.num_blocks, wl.scale))
     assert np.array_equal(out[1], np.zeros((2, 8)))
     assert np.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
+# fp8 caches: dequantise on read ("kv-cache-memory-core", section 4.4, and
+# "vLLM intro part 2", section 7: the cache stores fp8 codes, a read widens a
+# code and multiplies it by the tensor's scale).  The reference side decodes
+# the codes with torch's float8 types -- not the oracle's codec -- and the K
+# and V scales differ by a factor of 85, so using one for the other, or
+# dropping either, moves the result far outside the comparison bound.
+# ---------------------------------------------------------------------------
+FP8_TORCH = {"fp8_e4m3": torch.float8_e4m3fn, "fp8_e5m2": torch.float8_e5m2}
+K_SCALE, V_SCALE = 0.02, 1.7
+
+
+def _fp8_codes(kind, shape, gen):
+    """Codes of N(0, 16^2) values cast by torch (round to nearest, finite
+    for both formats at this magnitude)."""
+    x = torch.randn(shape, generator=gen) * 16.0
+    return x.to(FP8_TORCH[kind]).view(torch.uint8).numpy()
+
+
+def _fp8_contiguous(kind, lens, Hq, Hkv, D, bs, seed):
+    """A pool of fp8 codes whose tables are the identity, and bf16 queries;
+    returns (q raw, k codes, v codes, tables, seq_lens, NB)."""
+    gen = torch.Generator().manual_seed(seed)
+    nblk = [-(-L // bs) for L in lens]
+    NB = sum(nblk)
+    k = _fp8_codes(kind, (NB, bs, Hkv, D), gen)
+    v = _fp8_codes(kind, (NB, bs, Hkv, D), gen)
+    MB = max(nblk)
+    bt = np.full((len(lens), MB), -1, dtype=np.int32)
+    start = 0
+    for i, n in enumerate(nblk):
+        bt[i, :n] = np.arange(start, start + n)
+        start += n
+    q = torch.randn(len(lens), Hq, D, generator=gen).to(torch.bfloat16)
+    return oracle.as_raw(q), k, v, bt, np.array(lens, dtype=np.int32), NB
+
+
+def _fp8_dense_reference(kind, q_raw, k, v, lens, Hq, Hkv, D, bs, k_scale, v_scale):
+    """Dense attention over the contiguous pool: codes widened by torch,
+    times the scale, then numpy."""
+    to64 = lambda a: torch.from_numpy(a).view(FP8_TORCH[kind]).to(torch.float64).numpy()
+    qd = torch.from_numpy(q_raw.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    # the interface passes the scales as float32
+    K = to64(k).reshape(-1, Hkv, D) * float(np.float32(k_scale))
+    V = to64(v).reshape(-1, Hkv, D) * float(np.float32(v_scale))
+    out, start = [], 0
+    for i, L in enumerate(lens):
+        out.append(_dense_from_contiguous(qd[i], K[start:start + L], V[start:start + L],
+                                          float(np.float32(1.0 / math.sqrt(D))), Hq // Hkv))
+        start += -(-int(L) // bs) * bs
+    return np.stack(out)
+
+
+def _fp8_oracle(kind, q_raw, k, v, bt, lens, Hq, Hkv, D, bs, NB, k_scale, v_scale):
+    p = oracle.Problem(q_raw, oracle.BF16, k, v, oracle.DTYPE_CODES[kind], bt, lens, Hq, Hkv, D, bs, NB,
+                       1.0 / math.sqrt(D), k_scale, v_scale)
+    return oracle.decode(p)
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "fp8_e5m2"])
+def test_oracle_fp8_dequantise_on_read_matches_dense(kind):
+    lens = [1, 15, 16, 17, 40, 100]
+    Hq, Hkv, D, bs = 8, 2, 64, 16
+    q, k, v, bt, sl, NB = _fp8_contiguous(kind, lens, Hq, Hkv, D, bs, seed=31)
+    got = _fp8_oracle(kind, q, k, v, bt, sl, Hq, Hkv, D, bs, NB, K_SCALE, V_SCALE)
+    want = _fp8_dense_reference(kind, q, k, v, lens, Hq, Hkv, D, bs, K_SCALE, V_SCALE)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    # L = 1 reads exactly v_scale times the one value code
+    assert np.array_equal(got[0], want[0])
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("mistake", ["scales_swapped", "k_scale_dropped", "v_scale_dropped"])
+def test_oracle_fp8_planted_scale_mistakes_are_caught(kind, mistake):
+    """The dense check above fails when the oracle is handed the scales the
+    way a plausible mistake would use them."""
+    lens = [9, 33, 70]
+    Hq, Hkv, D, bs = 4, 2, 64, 16
+    q, k, v, bt, sl, NB = _fp8_contiguous(kind, lens, Hq, Hkv, D, bs, seed=32)
+    ks, vs = {"scales_swapped": (V_SCALE, K_SCALE), "k_scale_dropped": (1.0, V_SCALE),
+              "v_scale_dropped": (K_SCALE, 1.0)}[mistake]
+    bad = _fp8_oracle(kind, q, k, v, bt, sl, Hq, Hkv, D, bs, NB, ks, vs)
+    want = _fp8_dense_reference(kind, q, k, v, lens, Hq, Hkv, D, bs, K_SCALE, V_SCALE)
+    err = np.abs(bad - want).max(axis=-1)                  # per (sequence, head)
+    bound = 6e-2 + 6e-2 * np.abs(want).max(axis=-1)       # the GPU comparison's fp8 bound
+    assert (err > bound).all(), (mistake, err.min(), bound.max())
+
+
+def test_threaded_oracle_equals_decode():
+    """The full-size GPU comparisons run oracle.attend_one per (sequence,
+    head) on several host threads; that gives oracle.decode's values bit for
+    bit."""
+    from _harness import oracle_decode_threaded
+    wl = inputs.make_random([1, 17, 300, 45, 1000], num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                            kv_dtype="fp8_e4m3", q_dtype="bf16", seed=33, v_mult=16.0)
+    k, v = _written(wl)
+    p = _problem_raw(wl, k, v, wl.block_tables)
+    assert np.array_equal(oracle_decode_threaded(p, threads=4), oracle.decode(p))
