@@ -90,8 +90,8 @@ const char* pa_last_error_detail(void);
  * partition_tokens is the value that will be passed to pa_decode.
  * Returns 0 for invalid arguments.
  */
-size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
-                                int max_seq_len, int partition_tokens);
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_seq_len,
+                                int head_dim, int partition_tokens);
 
 /*
  * pa_decode -- single-query decode attention over a paged KV pool
@@ -125,7 +125,9 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
  * as two e4m3 terms, 8 significant bits (exact for bf16 queries, except
  * elements below 2^-9 of the largest in their GQA group); an infinite query
  * element saturates to +-448 there instead of propagating.  pa_decode_simt
- * keeps everything in fp32.
+ * keeps everything in fp32.  f32 caches (with f32 q) run on CUDA-core
+ * FMAs in fp32 throughout: fp32 is no tensor-core operand type here, so that
+ * kernel is the only one for them.
  *   workspace         device buffer of at least pa_decode_workspace_size(...)
  *                     bytes, 256-byte aligned; contents need no initialisation
  *                     and are scratch between calls.  Calls sharing one
@@ -144,8 +146,9 @@ pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype,
 
 /*
  * pa_decode_simt -- the same operation, arguments and results as pa_decode,
- * computed with CUDA-core FMAs instead of tensor-core MMAs.  It is the path
- * for f32 caches and a measured comparison point for the others.
+ * computed with CUDA-core FMAs instead of tensor-core MMAs, for every cache
+ * type.  pa_decode runs this kernel for f32 caches; for the other types it
+ * is a measured comparison point.
  */
 pa_status pa_decode_simt(void* out, const void* q, pa_dtype q_dtype,
                          const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
@@ -236,8 +239,8 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype kv_dtype,
  * Tensor cores only (f16, bf16 and fp8 caches); other arguments as for
  * pa_decode.  With every n_i = 1 the result equals pa_decode's.
  */
-size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int head_dim,
-                                   int max_seq_len, int partition_tokens);
+size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int max_seq_len,
+                                   int head_dim, int partition_tokens);
 pa_status pa_attention(void* out, const void* q, pa_dtype q_dtype,
                        const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
                        const int32_t* block_tables, int max_blocks_per_seq,

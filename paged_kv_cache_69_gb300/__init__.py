@@ -153,14 +153,14 @@ def _flag(err_flag: Optional[torch.Tensor]):
 
 
 # ---------------------------------------------------------------------------
-def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int,
+def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, max_seq_len: int, head_dim: int,
                              partition_tokens: int = 0) -> int:
-    return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens))
+    return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, max_seq_len, head_dim, partition_tokens))
 
 
-def alloc_workspace(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int,
+def alloc_workspace(num_seqs: int, num_q_heads: int, max_seq_len: int, head_dim: int,
                     partition_tokens: int = 0, device=None) -> torch.Tensor:
-    n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens)
+    n = pa_decode_workspace_size(num_seqs, num_q_heads, max_seq_len, head_dim, partition_tokens)
     if n == 0:
         raise PaError(1, "invalid workspace bounds")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")   # torch allocations are 256-B aligned
@@ -185,7 +185,7 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
     _flag(err_flag)
     MB = block_tables.shape[1]
     if workspace is None:
-        workspace = alloc_workspace(B, Hq, D, MB * bs, partition_tokens, device=q.device)
+        workspace = alloc_workspace(B, Hq, MB * bs, D, partition_tokens, device=q.device)
     fn = lib().pa_decode_simt if simt else lib().pa_decode
     _check(fn(_ptr(out), _ptr(q), _code(q), _ptr(k_cache), _ptr(v_cache), _code(k_cache, kv_dtype),
               _ptr(block_tables), MB, _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, float(scale),
@@ -291,9 +291,9 @@ def pa_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor
                                 Hkv, D, bs, _ptr(err_flag), _stream(stream)))
 
 
-def pa_attention_workspace_size(num_seqs: int, max_q_len: int, num_q_heads: int, head_dim: int,
-                                max_seq_len: int, partition_tokens: int = 0) -> int:
-    return int(lib().pa_attention_workspace_size(num_seqs, max_q_len, num_q_heads, head_dim, max_seq_len,
+def pa_attention_workspace_size(num_seqs: int, max_q_len: int, num_q_heads: int, max_seq_len: int,
+                                head_dim: int, partition_tokens: int = 0) -> int:
+    return int(lib().pa_attention_workspace_size(num_seqs, max_q_len, num_q_heads, max_seq_len, head_dim,
                                                  partition_tokens))
 
 
@@ -319,7 +319,7 @@ def pa_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
         raise ValueError("q_start must be int32 with num_seqs + 1 entries")
     MB = block_tables.shape[1]
     if workspace is None:
-        n = pa_attention_workspace_size(B, max_q_len, Hq, D, MB * bs, partition_tokens)
+        n = pa_attention_workspace_size(B, max_q_len, Hq, MB * bs, D, partition_tokens)
         if n == 0:
             raise PaError(1, "invalid workspace bounds")
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)

@@ -176,8 +176,12 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     } else if (q_dtype != kv_dtype) {
         return fail(PA_ERR_UNSUPPORTED, "decode: q dtype must equal the cache dtype (fp8 caches excepted)");
     }
-    if (tc && kv_dtype == PA_F32)
-        return fail(PA_ERR_UNSUPPORTED, "decode: f32 caches run on the CUDA-core path (pa_decode_simt)");
+    // f32 caches: the CUDA-core kernel is the only one for that element type
+    // (fp32 is no tensor-core operand type here), so pa_decode runs it.
+    if (kv_dtype == PA_F32) {
+        if (mq) return fail(PA_ERR_UNSUPPORTED, "attention: f32 caches take one query token per sequence (pa_decode)");
+        tc = false;
+    }
     if (mq && (!tc || QL < 1 || total_q < 0 || static_cast<long long>(QL) * (Hq / Hkv) > 128))
         return fail(PA_ERR_UNSUPPORTED,
                     "attention: several query tokens need the tensor-core path and max_q_len * G <= 128");
@@ -421,7 +425,7 @@ extern "C" const char* pa_status_string(pa_status s) {
 
 extern "C" const char* pa_last_error_detail(void) { return g_detail; }
 
-extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_seq_len, int head_dim,
                                            int partition_tokens) {
     if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 || partition_tokens < 0)
         return 0;
@@ -454,8 +458,8 @@ extern "C" pa_status pa_decode_simt(void* out, const void* q, pa_dtype q_dtype, 
                        k_scale, v_scale, partition_tokens, workspace, workspace_bytes, err_flag, stream);
 }
 
-extern "C" size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int head_dim,
-                                              int max_seq_len, int partition_tokens) {
+extern "C" size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int max_seq_len,
+                                              int head_dim, int partition_tokens) {
     if (num_seqs < 0 || max_q_len <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
         partition_tokens < 0)
         return 0;

@@ -74,8 +74,8 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, pa_dtype q_dtyp
     int dev = 0;
     const cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return fail_cuda("decode_noalloc: no current device", de);
-    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
-                                                 max_blocks_per_seq * block_size, partition_tokens);
+    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq * block_size,
+                                                 head_dim, partition_tokens);
     if (need == 0) return fail(PA_ERR_INVALID_ARG, "decode_noalloc: invalid sizes for the scratch bound");
     if (need > kNoallocScratchBytes) {
         char msg[200];

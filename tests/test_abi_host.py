@@ -124,7 +124,7 @@ def _attention_args(**over):
     (dict(TQ=-1), 1),                           # negative total
     (dict(Hq=5), 1),                            # checks shared with decode
     (dict(D=96), 2),
-    (dict(kvd=pa.PA_F32, qd=pa.PA_F32), 2),     # tensor cores only: no f32 cache
+    (dict(kvd=pa.PA_F32, qd=pa.PA_F32), 2),     # several query tokens: no f32 cache
 ])
 def test_attention_host_validation(lib, over, status):
     assert lib.pa_attention(*_attention_args(**over)) == status
@@ -137,10 +137,10 @@ def test_attention_without_query_tokens_is_a_noop(lib):
 
 
 def test_workspace_sizes_reject_bad_sizes(lib):
-    assert lib.pa_decode_workspace_size(-1, 4, 128, 100, 0) == 0
-    assert lib.pa_decode_workspace_size(2, 0, 128, 100, 0) == 0
-    assert lib.pa_attention_workspace_size(2, 0, 4, 128, 100, 0) == 0
-    assert lib.pa_attention_workspace_size(2, 2, 4, 128, -5, 0) == 0
+    assert lib.pa_decode_workspace_size(-1, 4, 100, 128, 0) == 0
+    assert lib.pa_decode_workspace_size(2, 0, 100, 128, 0) == 0
+    assert lib.pa_attention_workspace_size(2, 0, 4, 100, 128, 0) == 0
+    assert lib.pa_attention_workspace_size(2, 2, 4, -5, 128, 0) == 0
 
 
 def test_noalloc_host_validation(lib):

@@ -41,7 +41,7 @@ def test_decode_passes_the_sizes(rec):
     q, out, bt, sl = _decode_inputs()
     pa.pa_decode(out, q, k, v, bt, sl, 0.125, partition_tokens=32)
     (n0, a0), (n1, a1) = rec.calls
-    assert n0 == "pa_decode_workspace_size" and a0 == (3, 4, 64, 5 * 16, 32)
+    assert n0 == "pa_decode_workspace_size" and a0 == (3, 4, 5 * 16, 64, 32)
     assert n1 == "pa_decode"
     # q_dtype, kv_dtype, MB, B, Hq, Hkv, D, bs, NB, scale, partition, workspace bytes
     assert (a1[2], a1[5], a1[7], a1[9], a1[10], a1[11], a1[12], a1[13], a1[14]) == \
@@ -172,7 +172,7 @@ def test_attention_sizes_and_checks(rec):
     qs = torch.tensor([0, 2, 6, 9], dtype=torch.int32)
     pa.pa_attention(out, q, k, v, bt, sl, qs, 0.1, 4)
     (n0, a0), (n1, a1) = rec.calls
-    assert n0 == "pa_attention_workspace_size" and a0 == (3, 4, 4, 64, 80, 0)
+    assert n0 == "pa_attention_workspace_size" and a0 == (3, 4, 4, 80, 64, 0)
     # MB, B, total_q, max_q_len, Hq, Hkv, D, bs, NB
     assert (a1[7], a1[10], a1[11], a1[12], a1[13], a1[14], a1[15], a1[16], a1[17]) == \
         (5, 3, 9, 4, 4, 2, 64, 16, 10)

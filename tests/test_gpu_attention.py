@@ -67,6 +67,21 @@ def test_attention_matches_oracle(case):
     compare(out, ref, wl.kv_dtype, wl.name)
 
 
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "fp8_e5m2"])
+def test_attention_fp8_unequal_k_and_v_scales(kv):
+    """v_scale / k_scale about 16: a swapped or dropped scale fails."""
+    nq = [3, 6, 1]
+    wl = inputs.make_random([40, 700, 2500], num_q_heads=28, num_kv_heads=4, head_dim=128, block_size=16,
+                            kv_dtype=kv, q_dtype="bf16", spare_blocks=9, seed=91, v_mult=16.0,
+                            name=f"mq_{kv}_unequal_scales")
+    assert wl.v_scale / wl.k_scale > 10
+    g = torch.Generator().manual_seed(191)
+    q = torch.randn(sum(nq), 28, 128, generator=g).to(torch.bfloat16)
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(nq)]), dtype=torch.int32)
+    out, ref, _ = _run(wl, q, qs, nq)
+    compare(out, ref, wl.kv_dtype, wl.name)
+
+
 def test_sequences_without_keys_or_with_fewer_keys_than_queries():
     """A sequence with no keys gives zero rows for all its query tokens (and
     leaves the other sequences' rows alone); with fewer keys than query

@@ -78,9 +78,11 @@ def test_copy_blocks_bit_exact(kv):
 
 
 @pytest.mark.slow
-def test_fp8_quantiser_all_float32_bit_patterns():
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "fp8_e5m2"])
+def test_fp8_quantiser_all_float32_bit_patterns(kv):
     """Every one of the 2^32 float32 bit patterns, quantised by the cache
-    write with scale 1, equals the oracle's E4M3 encoding."""
+    write with scale 1, equals the oracle's E4M3 (resp. E5M2) encoding."""
+    encode = oracle.encode_e4m3 if kv == "fp8_e4m3" else oracle.encode_e5m2
     Hkv, D = 1, 64
     n = 1 << 26
     T = n // (Hkv * D)
@@ -93,9 +95,9 @@ def test_fp8_quantiser_all_float32_bit_patterns():
         bits = np.arange(c * n, (c + 1) * n, dtype=np.uint64).astype(np.uint32)
         x = bits.view(np.float32).reshape(T, Hkv, D)
         xt = torch.from_numpy(x).cuda()
-        pa.pa_reshape_and_cache(kc, vc, xt, xt, slots, kv_dtype="fp8_e4m3", k_scale=1.0, v_scale=1.0)
+        pa.pa_reshape_and_cache(kc, vc, xt, xt, slots, kv_dtype=kv, k_scale=1.0, v_scale=1.0)
         got = kc.view(-1).cpu().numpy()
-        want = oracle.encode_e4m3(x.reshape(-1), 1.0)
+        want = encode(x.reshape(-1), 1.0)
         bad = np.nonzero(got != want)[0]
         assert bad.size == 0, (f"chunk {c}: {bad.size} mismatches, first input bits "
                                f"{hex(int(bits[bad[0]]))} gpu {got[bad[0]]:#x} oracle {want[bad[0]]:#x}")

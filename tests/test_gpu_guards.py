@@ -71,7 +71,7 @@ def test_cache_write_copy_and_decode_stay_in_bounds(kv, qd):
     # decode into a guarded output and a guarded workspace, with and without partitions
     MB = d.block_tables.shape[1]
     for pt in (0, 32):
-        ws0 = pa.alloc_workspace(d.num_seqs, d.num_q_heads, d.head_dim, MB * d.block_size, pt)
+        ws0 = pa.alloc_workspace(d.num_seqs, d.num_q_heads, MB * d.block_size, d.head_dim, pt)
         wbuf, ws = guarded_like(torch.zeros_like(ws0))
         obuf, out = guarded_like(torch.zeros_like(d.q))
         pa.pa_decode(out, d.q, k, v, d.block_tables, d.seq_lens, d.scale, k_scale=d.k_scale, v_scale=d.v_scale,
@@ -95,7 +95,7 @@ def test_attention_and_swap_stay_in_bounds():
     q = torch.randn(sum(nq), 28, 128, generator=g).half().cuda()
     qs = torch.tensor([0, 3, 4, 9], dtype=torch.int32, device="cuda")
     MB = d.block_tables.shape[1]
-    n = pa.pa_attention_workspace_size(d.num_seqs, max(nq), 28, 128, MB * d.block_size, 0)
+    n = pa.pa_attention_workspace_size(d.num_seqs, max(nq), 28, MB * d.block_size, 128, 0)
     wbuf, ws = guarded_like(torch.zeros(n, dtype=torch.uint8, device="cuda"))
     obuf, out = guarded_like(torch.zeros_like(q))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")

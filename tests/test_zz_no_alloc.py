@@ -2,16 +2,19 @@
 (for example a serving loop whose device memory is fully pre-partitioned by
 its own allocator, or a plugin whose host framework owns all device memory).
 Its partials go to scratch memory built into the library.  Through the C
-interface, two calls in a row must match pa_decode with a caller workspace,
-within the decode tolerance; an oversized batch must be refused up front.
-This file runs last so that a failure here leaves every other test run."""
+interface, two calls in a row must give exactly pa_decode's output with a
+caller workspace (the same kernels run the same schedule) and match the
+oracle within the decode tolerance; an oversized batch must be refused up
+front.  This file runs last so that a failure here leaves every other test
+run."""
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_69_gb300 as pa
 from paged_kv_cache_69_gb300 import inputs
 
-from _harness import GpuStep, TOL
+from _harness import GpuStep, compare, oracle_caches, oracle_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -28,24 +31,26 @@ def _built():
 ], ids=["fp16_gqa7", "bf16_long"])
 def test_noalloc_matches_workspace_decode_twice(make):
     wl = make()
+    ref_k, ref_v = oracle_caches(wl)
+    want = oracle.decode(oracle_problem(wl, ref_k, ref_v))
     step = GpuStep(wl)
     step.setup()
     step.write_step()
     ref = step.decode().clone()
     torch.cuda.synchronize()
     d = step.dev
-    tol = TOL[wl.kv_dtype]
     for _ in range(2):
         out = torch.full_like(ref, float("nan"))
         pa.pa_decode_noalloc(out, d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.scale,
                              k_scale=d.k_scale, v_scale=d.v_scale, err_flag=step.err)
         torch.cuda.synchronize()
         assert step.err.item() == 0
-        torch.testing.assert_close(out.float(), ref.float(), atol=tol["atol"], rtol=tol["rtol"])
+        assert torch.equal(out, ref), "pa_decode_noalloc differs from pa_decode with a caller workspace"
+        compare(out, want, wl.kv_dtype, wl.name)
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch():
-    need = pa.pa_decode_workspace_size(100000, 64, 128, 4096, 0)
+    need = pa.pa_decode_workspace_size(100000, 64, 4096, 128, 0)
     assert need > pa.NOALLOC_SCRATCH_BYTES
     q = torch.empty((1, 64, 128), dtype=torch.float16, device="cuda")
     kc = torch.empty((1, 16, 8, 128), dtype=torch.float16, device="cuda")
