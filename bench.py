@@ -205,6 +205,34 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline leg and reference arm)
 # ---------------------------------------------------------------------------
+def host_cpu() -> dict:
+    """The host's logical CPU count and CPU model name."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            import subprocess
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+
 def oracle_inputs(wl):
     import oracle
     k = oracle.as_raw(wl.k_cache).copy()
@@ -271,7 +299,8 @@ def run_reference(args) -> dict:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(wl, {"sample_seqs_per_step": per_step}),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             **host_cpu()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -307,7 +336,7 @@ def run_ours(args, rank, world, local) -> dict | None:
                         "gbs": nbytes / (fa.elapsed_time(fb) / 1e3) / 1e9}
     out = torch.empty_like(d.q)
     MB = d.block_tables.shape[1]
-    ws = pa.alloc_workspace(d.num_seqs, d.num_q_heads, d.head_dim, MB * d.block_size, args.partition_tokens,
+    ws = pa.alloc_workspace(d.num_seqs, d.num_q_heads, MB * d.block_size, d.head_dim, args.partition_tokens,
                             device=device)
     NQ = max(1, args.q_per_seq)
     if NQ > 1:
@@ -317,7 +346,7 @@ def run_ours(args, rank, world, local) -> dict | None:
         q_mq = torch.randn(d.num_seqs * NQ, d.num_q_heads, d.head_dim, generator=gq, device=device).to(d.q.dtype)
         out_mq = torch.empty_like(q_mq)
         qs_mq = torch.arange(0, d.num_seqs * NQ + 1, NQ, dtype=torch.int32, device=device)
-        ws = torch.empty(pa.pa_attention_workspace_size(d.num_seqs, NQ, d.num_q_heads, d.head_dim, MB * d.block_size,
+        ws = torch.empty(pa.pa_attention_workspace_size(d.num_seqs, NQ, d.num_q_heads, MB * d.block_size, d.head_dim,
                                                         args.partition_tokens), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
     pairs = d.cow_pairs if (d.cow_pairs is not None and d.cow_pairs.numel()) else None
@@ -374,9 +403,18 @@ def run_ours(args, rank, world, local) -> dict | None:
         g_start, g_end = t_start, t_end
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-    # K eager steps with events around each kernel: the per-kernel times
-    # (and the step time when no graph is used)
-    for i in range(K):
+    # Eager steps with events around each kernel: the per-kernel times (and
+    # the step time when no graph is used).  Per-call times are medians over
+    # at least 200 calls and about 0.5 s of work, so the clock sampler sees
+    # the GPU under load for many samples.
+    n_eager = K
+    if graph is not None:
+        step_ms = max(g_start.elapsed_time(g_end), 1e-3) / K
+        n_eager = int(min(20000, max(K, 200, math.ceil(500.0 / step_ms))))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_eager)]
+        ew = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_eager)]
+        ec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_eager)]
+    for i in range(n_eager):
         if pairs is not None:
             ec[i][0].record(stream)
             pa.pa_copy_blocks(d.k_cache, d.v_cache, pairs, err_flag=err)
@@ -393,9 +431,9 @@ def run_ours(args, rank, world, local) -> dict | None:
     if world > 1:
         dist.barrier()
     ms_total = g_start.elapsed_time(g_end) if graph is not None else t_start.elapsed_time(t_end)
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    write_us = statistics.mean(a.elapsed_time(b) for a, b in ew) * 1e3
-    copy_us = statistics.mean(a.elapsed_time(b) for a, b in ec) * 1e3 if pairs is not None else None
+    dec_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    write_us = statistics.median(a.elapsed_time(b) for a, b in ew) * 1e3
+    copy_us = statistics.median(a.elapsed_time(b) for a, b in ec) * 1e3 if pairs is not None else None
     ms_total, dec_ms = max_over_ranks([ms_total, dec_ms], device, world)
     if err.item() != 0:
         raise RuntimeError(f"device error flag {err.item()} during the benchmark")
@@ -465,7 +503,7 @@ def run_ours(args, rank, world, local) -> dict | None:
                         "frac": achieved / peak, "peak_source": peak_src,
                         "kernel": "pa_decode (main + reduce)" if NQ == 1 else "pa_attention (main + reduce)",
                         "algorithmic_bytes_per_launch": alg,
-                        "launch_ms": dec_ms,
+                        "launch_ms": dec_ms, "launch_ms_stat": f"median of {n_eager} eager calls",
                         "traffic": profile_traffic(args.workload) if NQ == 1 and not args.partition_tokens else None},
            "gpu_launches": K * (3 + (1 if pairs is not None else 0)),
            "clocks": clk, "e2e": e2e,
@@ -478,7 +516,8 @@ def run_ours(args, rank, world, local) -> dict | None:
         rate, n, el = time_oracle(wl.to("cpu"), budget_s=args.cpu_budget)
         res["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                "sample": f"first {n} of {wl.num_seqs} sequences (all {wl.num_q_heads} query "
-                                         f"heads, cache write + decode), {el:.1f} s, one thread"}
+                                         f"heads, cache write + decode), {el:.1f} s, one thread",
+                               **host_cpu()}
     return res
 
 
