@@ -190,9 +190,17 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     // tokens); other fp8 shapes convert e4m3 to f16 in registers.
     const bool native8 = !mq && tc && is_fp8(kv_dtype) && D == 128 && Hq / Hkv <= 8 &&
                          partition_tokens % 32 == 0;
-    const int CT = native8 ? 32 : 16;
     const bool fp8t = native8 && Hq / Hkv <= 4;      // keys as the MMA rows: half the MMAs
-    const void* kern = mq      ? decode_kernel_mq(kv_dtype, q_dtype, D)
+    // Several query tokens with 96-128 (token, head) rows per KV head on a
+    // 16-bit cache: the tcgen05 kernel, all rows of a KV head in one 128-row
+    // tile with the accumulators in tensor memory, 32-token chunks.  (With
+    // fewer rows only some of its warps hold rows and the per-row softmax
+    // runs serially; the mma.sync kernel is faster there.)
+    const bool um = mq && !is_fp8(kv_dtype) && QL * (Hq / Hkv) >= 96 && QL * (Hq / Hkv) <= 128 &&
+                    partition_tokens % 32 == 0;
+    const int CT = (native8 || um) ? 32 : 16;
+    const void* kern = um      ? decode_kernel_mq_um(kv_dtype, q_dtype, D)
+                       : mq    ? decode_kernel_mq(kv_dtype, q_dtype, D)
                        : fp8t  ? decode_kernel_fp8t(kv_dtype, q_dtype, D)
                        : native8 ? decode_kernel_e4m3(kv_dtype, q_dtype, D)
                        : tc    ? decode_kernel_tc(kv_dtype, q_dtype, D)
@@ -223,9 +231,12 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         HPC = h;
         break;
     }
+    if (um) HPC = 1;                 // one KV head per CTA: its rows fill the tile
     if (HPC == 0) return fail(PA_ERR_UNSUPPORTED, "decode: no head grouping fits one CTA");
     const int NHG = Hkv / HPC;
-    const int NCW = HPC * MT;
+    // tcgen05 path: 4 consumer warps (one tile row per thread), the producer
+    // warp and the MMA warp
+    const int NCW = um ? 4 : HPC * MT;
     const int rpb = std::min(CT, bs);
     const int DH = D * e / 128;
     if (DH < 1 || (D * e) % 128 != 0) return fail(PA_ERR_UNSUPPORTED, "decode: head_dim * elem bytes must be a multiple of 128");
@@ -250,12 +261,22 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.kv_bytes = static_cast<uint32_t>(CT * HPC * D * e);
     p.q_bytes = static_cast<uint32_t>(QL * HPC * G * D * eq);
     p.q_slot_bytes = (p.q_bytes + 1023u) & ~1023u;   // swizzled tensor copies need 1024-B alignment
+    if (um) {
+        // column planes of the query rows 1024-B aligned.  The MMA reads 128
+        // rows from every plane; the rows past the valid ones may fall in the
+        // next plane, slot or the P buffers after the ring -- shared memory
+        // of this CTA whose values only reach tile rows that are never used.
+        p.q_plane_bytes = static_cast<uint32_t>((QL * G * 128 + 1023) & ~1023);
+        p.q_slot_bytes = static_cast<uint32_t>(DH) * p.q_plane_bytes;
+    }
     p.stage_bytes = 2 * p.kv_bytes;
     // CUDA-core variant: private fp32 query rows; transposed fp8: P bytes per warp
-    const uint32_t simtq = fp8t ? static_cast<uint32_t>(NCW * 256) : tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
+    // tcgen05 path: two P buffers of 128 rows x 32 tokens
+    const uint32_t simtq = um ? 2u * 128u * 32u * 2u
+                         : fp8t ? static_cast<uint32_t>(NCW * 256) : tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
     const uint32_t extras = 1024;   // barriers, stage descriptors, prologue scratch
     const uint32_t fixed = NQ * p.q_slot_bytes + simtq + extras + 1024;   // + base alignment slack
-    const int threads = (NCW + 1) * 32;
+    const int threads = (NCW + (um ? 2 : 1)) * 32;
     // Two co-resident CTAs per SM double the consumer warps that hide the
     // per-chunk MMA/softmax latency; use them when registers and shared
     // memory allow at least 3 stages each, else one CTA with a deeper ring.
@@ -331,7 +352,8 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         const cuuint32_t dhq = static_cast<cuuint32_t>(D * eq / 128);
         cuuint64_t dims[4] = {e128q, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(std::max(total_q, 1)), dhq};
         cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * eq, static_cast<cuuint64_t>(Hq) * D * eq, 128};
-        cuuint32_t box[4] = {e128q, static_cast<cuuint32_t>(HPC * G), static_cast<cuuint32_t>(QL), dhq};
+        // tcgen05 path: one column plane per copy
+        cuuint32_t box[4] = {e128q, static_cast<cuuint32_t>(HPC * G), static_cast<cuuint32_t>(QL), um ? 1u : dhq};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (!enc || HPC * G > 256 || QL > 256 ||
             enc(&tq, tmap_type(q_dtype), 4, const_cast<void*>(q), dims, strides, box, es,

@@ -1,5 +1,6 @@
 // pa_attention.cu -- instantiations of the paged attention kernel for
-// several query tokens per sequence (causal), tensor-core variant.
+// several query tokens per sequence (causal): the mma.sync variant and the
+// tcgen05 variant (accumulators in tensor memory) for 16-bit caches.
 #include <cuda.h>
 
 #include "pa_decode_kernel.cuh"
@@ -15,6 +16,14 @@ const void* decode_kernel_mq(pa_dtype kv, pa_dtype q, int D) {
     if (kv == PA_FP8_E4M3) return q == PA_F16 ? PA_MQ(FP8T, F16T, 128) : q == PA_BF16 ? PA_MQ(FP8T, BF16T, 128) : nullptr;
     if (kv == PA_FP8_E5M2) return q == PA_F16 ? PA_MQ(E5M2T, F16T, 128) : q == PA_BF16 ? PA_MQ(E5M2T, BF16T, 128) : nullptr;
 #undef PA_MQ
+    return nullptr;
+}
+
+const void* decode_kernel_mq_um(pa_dtype kv, pa_dtype q, int D) {
+#define PA_UM(KVT, DD) reinterpret_cast<const void*>(&pa_decode_kernel<KVT, KVT, DD, true, 32, true, false, true>)
+    if (kv == PA_F16 && q == PA_F16) return D == 128 ? PA_UM(F16T, 128) : D == 64 ? PA_UM(F16T, 64) : nullptr;
+    if (kv == PA_BF16 && q == PA_BF16) return D == 128 ? PA_UM(BF16T, 128) : D == 64 ? PA_UM(BF16T, 64) : nullptr;
+#undef PA_UM
     return nullptr;
 }
 

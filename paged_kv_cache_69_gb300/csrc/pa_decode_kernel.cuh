@@ -52,7 +52,7 @@ struct StageDesc {
     int slot;
     uint32_t vmask;
     uint32_t flags;          // SEG_* bits; bits 16.. hold the sequence's query count
-    int qslot;               // query ring slot holding this segment's rows
+    int qslot;               // query ring slot of the segment's rows (valid at SEG_START chunks)
     int qrow0;               // row of the sequence's first query token in q / out
     int qpos0;               // its position in the sequence (queries are the last tokens)
 };
@@ -93,6 +93,7 @@ struct DecodeParams {
     uint32_t bar_off;         // offset of the barriers
     int per_head_copies;      // 1: one TMA copy per (head, 128-B column block)
     int q_tma;                // 1: query rows arrive by a 128-B-swizzled tensor copy
+    uint32_t q_plane_bytes;   // tcgen05 path: distance between the query slot's 128-B column planes
 };
 
 __device__ __forceinline__ int cdiv_i(int a, int b) { return (a + b - 1) / b; }
@@ -343,7 +344,17 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16*
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack2(v[0], v[1], true), pack2(v[2], v[3], true));
 }
 
-template <class KV, class QT, int D, bool TC, int CT, bool MQ = false, bool T8 = false>
+// Barriers and the tensor-memory base of the tcgen05 path (shared memory).
+struct UmBars {
+    uint64_t sfull[2];        // S of chunk k in tensor-memory buffer k % 2 (MMA commit)
+    uint64_t pfull[2];        // P of chunk k in shared-memory buffer k % 2 (one arrival per consumer warp)
+    uint64_t pvdone[2];       // P V of chunk k added to O (MMA commit): P buffer k % 2 free again
+    uint64_t ofree;           // a segment's O read out (one arrival per consumer warp)
+    uint64_t fin;             // every MMA of the CTA complete
+    uint32_t tmem;            // tensor-memory base address
+};
+
+template <class KV, class QT, int D, bool TC, int CT, bool MQ = false, bool T8 = false, bool UM = false>
 struct DecodeKernel {
     using KT = typename KV::T;
     using QE = typename QT::T;
@@ -351,7 +362,8 @@ struct DecodeKernel {
     // 32-token chunks are the native-e4m3 tensor-core variant (fp8 operands,
     // m16n8k32); every other variant runs 16-token chunks.
     static constexpr bool NATIVE8 = (CT == 32);
-    static_assert(CT == 16 || (CT == 32 && FP8 && TC && D == 128), "32-token chunks: fp8 tensor-core path only");
+    static_assert(CT == 16 || (CT == 32 && ((FP8 && TC && D == 128) || UM)),
+                  "32-token chunks: the fp8 tensor-core and the tcgen05 paths only");
     static constexpr bool KV_E5M2 = (KV::code == PA_FP8_E5M2);
     static constexpr int MAXB = CT / 8;       // TMA boxes per chunk at the smallest block size
     static constexpr bool MMA_BF16 = (KV::code == PA_BF16);   // fp8 runs in f16
@@ -359,6 +371,12 @@ struct DecodeKernel {
     static constexpr int KS = D / 16;         // 16-deep k-steps over head_dim
     static constexpr int ROWB = D * KV::bytes;  // bytes of one K/V row
     static constexpr int CPR = ROWB / 16;     // 16-byte chunks per row
+    static_assert(!UM || (MQ && TC && !FP8 && CT == 32), "tcgen05 path: several query tokens, 16-bit caches");
+    static constexpr int UM_M = 128;          // tcgen05 tile rows: (query token, head) rows of one KV head
+    static constexpr int UM_TCOLS = 256;      // tensor-memory columns per CTA: two S buffers, then O
+    static_assert(!UM || 2 * CT + D <= UM_TCOLS, "two S buffers and O fit the allocation");
+    static constexpr int UM_O = 2 * CT;       // first column of O
+    static constexpr uint32_t UM_PBUF = UM_M * CT * 2;   // bytes of one P buffer
 
     // ---------------- producer ----------------
     static __device__ void producer(const DecodeParams& p, const Plan& pl, int hg, uint8_t* base,
@@ -524,7 +542,14 @@ struct DecodeKernel {
                         const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
                             (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
                         uint8_t* qdst = base + p.q_off + qs * p.q_slot_bytes;
-                        if constexpr (MQ) {
+                        if constexpr (UM) {
+                            // one copy per 128-B column plane, planes q_plane_bytes
+                            // (a multiple of 1024) apart: the swizzle atoms of
+                            // every plane start aligned for the MMA descriptors
+#pragma unroll
+                            for (int dh = 0; dh < ROWB / 128; ++dh)
+                                tma_load_4d(qdst + dh * p.q_plane_bytes, tq, &full[slot], 0, hq0, qrow_i, dh);
+                        } else if constexpr (MQ) {
                             // rows [token][head] of QL tokens x HPC*G heads, one 4-D copy
                             tma_load_4d(qdst, tq, &full[slot], 0, hq0, qrow_i, 0);
                         } else {
@@ -1391,6 +1416,276 @@ struct DecodeKernel {
         }
     }
 
+    // ---------------- tcgen05 consumer (several query tokens per KV head) ----------------
+    // One KV head per CTA.  Its (query token, head) rows are the M = 128 rows
+    // of the tile: row r is tensor-memory lane r, owned by thread r of the
+    // consumer warps 0-3.  Per chunk the MMA warp computes S = Q K^T into one
+    // of two S buffers in tensor memory; each row's thread masks (sequence
+    // end, causal limit), exponentiates against a reference maximum and
+    // writes its weights to a K-major P buffer in shared memory (two,
+    // alternating); the MMA warp then adds P V into O (M x D fp32 in tensor
+    // memory) with V read in place from the stage as an MN-major operand.
+    // Chunks are 32 tokens (two 16-token MMA steps each way), so one
+    // producer iteration moves 16 KB of one head's K and V.
+    // The reference maximum moves only when a row's maximum passes it by more
+    // than 2^8, and only then is that row of O rescaled (tcgen05.ld / st), so
+    // acc, l and m of a partial all refer to it.  V rows of tokens outside the
+    // chunk's valid mask are zeroed in shared memory first: the MMA reads
+    // every row, and 0 x NaN is NaN.
+    static __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+    }
+
+    static __device__ void consumer_um(const DecodeParams& p, const Plan& pl, int hg, int w, uint8_t* base,
+                                       uint64_t* full, UmBars* ub, const StageDesc* descs) {
+        const int lane = threadIdx.x & 31;
+        const int R = w * 32 + lane;
+        const int rows = p.QL * p.G;
+        const int jrow = R / p.G;                         // query token of this row
+        const int head = hg * p.G + (R - jrow * p.G);     // one KV head per CTA
+        const uint32_t trow = ub->tmem + (static_cast<uint32_t>(w * 32) << 16);
+        const int S = p.stages;
+        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u, static_cast<uint32_t>(p.rpb) * 128u,
+                           p.rpb};
+        uint8_t* pbuf0 = base + p.simtq_off;
+        constexpr uint32_t FULLM = CT == 32 ? 0xffffffffu : ((1u << CT) - 1u);
+        float m_ref = -INFINITY, l = 0.f;
+        bool row_ok = false;
+        int lim = -1;
+        bool ok = true;
+        for (int st = 0, k = pl.cs; k < pl.ce; ++k, ++st) {
+            const int slot = st % S;
+            if (!(ok = warp_wait(&full[slot], (st / S) & 1u))) break;
+            const StageDesc d = descs[slot];
+            uint8_t* vbuf = base + slot * p.stage_bytes + p.kv_bytes;
+            if (d.flags & SEG_START) {
+                const int qn = static_cast<int>(d.flags >> QCOUNT_SHIFT);
+                row_ok = R < rows && jrow < qn;
+                lim = row_ok ? d.qpos0 + jrow : -1;
+                m_ref = -INFINITY;
+                l = 0.f;
+            }
+            if ((d.vmask & FULLM) != FULLM) {
+                for (int i = R; i < CT * CPR; i += UM_M) {
+                    const int t = i / CPR, c = i - t * CPR;
+                    if (!((d.vmask >> t) & 1u))
+                        *reinterpret_cast<uint4*>(vbuf + lay.chunk_addr(lay.row_base(t, 0), t, c)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // ---- this row's scores of the chunk ----
+            if (!(ok = warp_wait(&ub->sfull[st & 1], (st >> 1) & 1u))) break;
+            tc05_fence_after();
+            float s[CT];
+            {
+                float h0[16], h1[16];
+                tmem_ld16(trow + (st & 1) * CT, h0);
+                tmem_ld16(trow + (st & 1) * CT + 16, h1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) { s[t] = h0[t]; s[16 + t] = h1[t]; }
+            }
+            float alpha = 1.f;
+            bool resc = false;
+            if (row_ok) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int t = 0; t < CT; ++t) {
+                    const bool keep = ((d.vmask >> t) & 1u) && d.tok0 + t <= lim;
+                    s[t] = keep ? s[t] * p.qk_scale : -INFINITY;
+                    mx = fmaxf(mx, s[t]);
+                }
+                if (mx > m_ref + 8.f) {       // also the first finite maximum (m_ref = -inf: O is zero)
+                    if (m_ref != -INFINITY) {
+                        alpha = exp2f(m_ref - mx);
+                        resc = true;
+                        l *= alpha;
+                    }
+                    m_ref = mx;
+                }
+                float sum = 0.f;
+#pragma unroll
+                for (int t = 0; t < CT; ++t) {
+                    s[t] = m_ref == -INFINITY ? 0.f : ex2_approx(s[t] - m_ref);
+                    sum += s[t];
+                }
+                l += sum;
+            } else {
+#pragma unroll
+                for (int t = 0; t < CT; ++t) s[t] = 0.f;
+            }
+            // P buffer st % 2 is free once P V of chunk st - 2 is complete
+            if (st >= 2 && !(ok = warp_wait(&ub->pvdone[st & 1], ((st >> 1) - 1) & 1u))) break;
+            if (__any_sync(0xffffffffu, resc)) {
+                // rescale this warp's rows of O: P V of chunk st - 1 must be complete
+                if (!(ok = warp_wait(&ub->pvdone[(st - 1) & 1], ((st - 1) >> 1) & 1u))) break;
+                tc05_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float o[16];
+                    tmem_ld16(trow + UM_O + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] *= alpha;
+                    tmem_st16(trow + UM_O + c0, o);
+                }
+                tmem_wait_st();
+            }
+            // ---- P: row R as CT / 8 core-matrix rows of 8 tokens (16 bytes each) ----
+            uint8_t* pb = pbuf0 + (st & 1) * UM_PBUF;
+#pragma unroll
+            for (int kc = 0; kc < CT / 8; ++kc) {
+                const float* w = s + 8 * kc;
+                *reinterpret_cast<uint4*>(pb + (kc * (UM_M / 8) + (R >> 3)) * 128 + (R & 7) * 16) =
+                    make_uint4(pack2(w[0], w[1], MMA_BF16), pack2(w[2], w[3], MMA_BF16),
+                               pack2(w[4], w[5], MMA_BF16), pack2(w[6], w[7], MMA_BF16));
+            }
+            fence_proxy_async_smem();            // P and zeroed V rows visible to the tensor core
+            tc05_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ub->pfull[st & 1]);
+            if (d.flags & SEG_END) {
+                if (!(ok = warp_wait(&ub->pvdone[st & 1], (st >> 1) & 1u))) break;
+                tc05_fence_after();
+                finish_segment_um(p, d, trow, row_ok, jrow, head, m_ref, l);
+                tc05_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ub->ofree);
+            }
+        }
+        if (!ok && lane == 0) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+    }
+
+    // End of a segment on the tcgen05 path: this thread's row of O, normalised
+    // into the output when the segment covers the whole sequence, else the
+    // unnormalised partial (acc, m, l).
+    static __device__ __forceinline__ void finish_segment_um(const DecodeParams& p, const StageDesc& d, uint32_t trow,
+                                                             bool row_ok, int jrow, int head, float m, float l) {
+        const bool direct = (d.flags & DIRECT) != 0;
+        const bool store = row_ok && (direct || d.slot < p.max_slots);
+        const float sc = direct ? (l > 0.f ? p.v_scale / l : 0.f) : p.v_scale;
+        QE* orow = static_cast<QE*>(p.out) + (static_cast<size_t>(d.qrow0 + jrow) * p.Hq + head) * D;
+        const size_t prow = (static_cast<size_t>(d.slot) * p.QL + jrow) * p.Hq + head;
+        float* pacc = p.part_acc + prow * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            float o[16];
+            tmem_ld16(trow + UM_O + c0, o);
+            tmem_wait_ld();
+            if (store) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] *= sc;
+                if (direct) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+                    dst[0] = make_uint4(pack2(o[0], o[1], MMA_BF16), pack2(o[2], o[3], MMA_BF16),
+                                        pack2(o[4], o[5], MMA_BF16), pack2(o[6], o[7], MMA_BF16));
+                    dst[1] = make_uint4(pack2(o[8], o[9], MMA_BF16), pack2(o[10], o[11], MMA_BF16),
+                                        pack2(o[12], o[13], MMA_BF16), pack2(o[14], o[15], MMA_BF16));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(pacc + c0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
+            }
+        }
+        if (store && !direct) p.part_ml[prow] = make_float2(m, l);
+        if (row_ok && !direct && (d.flags & GAP) && d.slot + 1 < p.max_slots) {
+            // the slot a range end meeting a partition end skips: an empty partial
+            const size_t prow1 = prow + static_cast<size_t>(p.QL) * p.Hq;
+            float4* z = reinterpret_cast<float4*>(p.part_acc + prow1 * D);
+#pragma unroll 4
+            for (int i = 0; i < D / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.part_ml[prow1] = make_float2(-INFINITY, 0.f);
+        }
+    }
+
+    // The MMA warp's issuing thread.  S of chunk st + 1 is issued before P V
+    // of chunk st when its bytes have landed, so the scores of the next chunk
+    // are ready when the consumers finish the current one; otherwise P V of
+    // chunk st goes first and frees its stage without waiting for memory.
+    static __device__ void mma_um(const DecodeParams& p, const Plan& pl, uint8_t* base, uint64_t* full,
+                                  uint64_t* empty, uint64_t* qempty, UmBars* ub, const StageDesc* descs) {
+        const int S = p.stages;
+        const uint32_t tm = ub->tmem;
+        const uint32_t id_s = umma_idesc_f16(MMA_BF16, UM_M, 16, false, false);
+        const uint32_t id_o = umma_idesc_f16(MMA_BF16, UM_M, D, false, true);
+        // K and V of a stage: 8-token groups 1024 B apart inside a box of 16
+        // or more rows, one box apart with 8-row boxes; 64-element column
+        // blocks rpb * 128 B apart (one head per CTA)
+        const uint32_t grp = p.rpb == 8 ? p.box_bytes : 1024u;
+        const uint32_t dhs = static_cast<uint32_t>(p.rpb) * 128u;
+        const uint32_t pb0 = smem_u32(base + p.simtq_off);
+        // byte offset of token t0 (a multiple of 8) in a stage's K or V buffer
+        auto tok_off = [&](int t0) -> uint32_t {
+            return static_cast<uint32_t>(t0 / p.rpb) * p.box_bytes + static_cast<uint32_t>(t0 % p.rpb) * 128u;
+        };
+        bool ok = true;
+        int q_cur = 0;          // query ring slot of the current segment (descriptors name it at its first chunk)
+        // S of chunk st, its stage already landed
+        auto issue_s_ready = [&](int st) {
+            const int slot = st % S;
+            const StageDesc d = descs[slot];
+            if (d.flags & SEG_START) q_cur = d.qslot;
+            const uint32_t qb = smem_u32(base + p.q_off + q_cur * p.q_slot_bytes);
+            const uint32_t kb = smem_u32(base + slot * p.stage_bytes);
+            // S for tokens 16h .. 16h + 15 into columns 16h .. of the buffer
+#pragma unroll
+            for (int h = 0; h < CT / 16; ++h) {
+                const uint32_t kh = kb + tok_off(16 * h);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t plane = static_cast<uint32_t>(kk >> 2), within = static_cast<uint32_t>(kk & 3) * 32u;
+                    umma_f16(tm + (st & 1) * CT + 16 * h,
+                             umma_desc(qb + plane * p.q_plane_bytes + within, 16u, 1024u, 2u),
+                             umma_desc(kh + plane * dhs + within, 16u, grp, 2u), id_s, kk > 0);
+                }
+            }
+            umma_commit(&ub->sfull[st & 1]);
+            if (d.flags & SEG_END) umma_commit(&qempty[q_cur]);       // the segment's query rows are read
+        };
+        auto issue_s = [&](int st) -> bool {
+            const int slot = st % S;
+            if (!mbar_wait_bounded(&full[slot], (st / S) & 1u)) return false;
+            tc05_fence_after();
+            issue_s_ready(st);
+            return true;
+        };
+        const int n = pl.ce - pl.cs;
+        int seg = 0;
+        if (n > 0) ok = issue_s(0);
+        for (int st = 0; st < n && ok; ++st) {
+            const int slot = st % S;
+            const StageDesc d = descs[slot];
+            // S of the next chunk goes first when its data is already here:
+            // P V of this chunk must not wait for the next chunk's bytes
+            bool s_next = st + 1 >= n;
+            if (!s_next && mbar_test_wait(&full[(st + 1) % S], ((st + 1) / S) & 1u)) {
+                tc05_fence_after();
+                issue_s_ready(st + 1);
+                s_next = true;
+            }
+            if (!(ok = mbar_wait_bounded(&ub->pfull[st & 1], (st >> 1) & 1u))) break;
+            const bool first = (d.flags & SEG_START) != 0;
+            if (first && seg > 0 && !(ok = mbar_wait_bounded(&ub->ofree, (seg - 1) & 1u))) break;
+            if (first) ++seg;
+            tc05_fence_after();
+            const uint32_t vb = smem_u32(base + slot * p.stage_bytes + p.kv_bytes);
+            // O += P V, one 16-token K step at a time
+#pragma unroll
+            for (int h = 0; h < CT / 16; ++h)
+                umma_f16(tm + UM_O,
+                         umma_desc(pb0 + (st & 1) * UM_PBUF + h * 2u * (UM_M / 8) * 128u, (UM_M / 8) * 128u, 128u, 0u),
+                         umma_desc(vb + tok_off(16 * h), dhs, grp, 2u), id_o, !first || h > 0);
+            umma_commit(&ub->pvdone[st & 1]);
+            umma_commit(&empty[slot]);                                 // K and V of the stage are read
+            if (!s_next && !(ok = issue_s(st + 1))) break;
+        }
+        // nothing may still read shared or tensor memory when the CTA frees them
+        umma_commit(&ub->fin);
+        if (!mbar_wait_bounded(&ub->fin, 0u)) ok = false;
+        if (!ok) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
+    }
+
     // ---------------- CUDA-core consumer ----------------
     // Lanes (t, half) = (lane & 15, lane >> 4) compute the dot products of
     // token t over half of head_dim for up to 16 query rows; for P*V each
@@ -1579,11 +1874,11 @@ struct DecodeKernel {
     }
 };
 
-template <class KV, class QT, int D, bool TC, int CT, bool MQ = false, bool T8 = false>
+template <class KV, class QT, int D, bool TC, int CT, bool MQ = false, bool T8 = false, bool UM = false>
 __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
-    using K = DecodeKernel<KV, QT, D, TC, CT, MQ, T8>;
+    using K = DecodeKernel<KV, QT, D, TC, CT, MQ, T8, UM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + p.bar_off);
@@ -1594,6 +1889,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     int4* s_first = reinterpret_cast<int4*>(scratch + 32);
     int2* s_tot = reinterpret_cast<int2*>(s_first + 1);
     int* s_end = reinterpret_cast<int*>(s_tot + 1);
+    UmBars* ub = reinterpret_cast<UmBars*>((reinterpret_cast<uintptr_t>(s_end + 1) + 15) & ~uintptr_t(15));
 
     // This kernel is launched as a programmatic dependent of the previous
     // kernel on the stream (typically the cache write): its CTAs may be
@@ -1612,15 +1908,51 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
+        // on the tcgen05 path one MMA commit frees a stage or a query slot
+        const uint32_t frees = UM ? 1u : static_cast<uint32_t>(p.NCW);
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], p.NCW);
+            mbar_init(&empty[s], frees);
         }
-        for (int s = 0; s < NQ; ++s) mbar_init(&qempty[s], p.NCW);
+        for (int s = 0; s < NQ; ++s) mbar_init(&qempty[s], frees);
+        if constexpr (UM) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&ub->sfull[b], 1);
+                mbar_init(&ub->pfull[b], p.NCW);
+                mbar_init(&ub->pvdone[b], 1);
+            }
+            mbar_init(&ub->ofree, p.NCW);
+            mbar_init(&ub->fin, 1);
+        }
         fence_barrier_init();
         fence_proxy_async_smem();
     }
+    if constexpr (UM) {
+        if (warp == 0) tmem_alloc<K::UM_TCOLS>(&ub->tmem);
+        tc05_fence_before();
+    }
     __syncthreads();
+    if constexpr (UM) {
+        tc05_fence_after();
+        if (warp == p.NCW) {
+            if ((threadIdx.x & 31) == 0) {
+                prefetch_tensormap(&tk);
+                prefetch_tensormap(&tv);
+                prefetch_tensormap(&tq);
+            }
+            K::producer(p, pl, hg, base, full, empty, qempty, descs, &tk, &tv, &tq);
+        } else if (warp == p.NCW + 1) {
+            if ((threadIdx.x & 31) == 0) K::mma_um(p, pl, base, full, empty, qempty, ub, descs);
+        } else if (warp < p.NCW) {
+            K::consumer_um(p, pl, hg, warp, base, full, ub, descs);
+        }
+        // every role is done: the tensor memory goes back
+        tc05_fence_before();
+        __syncthreads();
+        tc05_fence_after();
+        if (warp == 0) tmem_dealloc<K::UM_TCOLS>(ub->tmem);
+        return;
+    }
     if (warp == p.NCW) {
         if ((threadIdx.x & 31) == 0) {
             prefetch_tensormap(&tk);
@@ -1679,7 +2011,10 @@ template <typename OutT, int D, int WPI>
 __global__ void __launch_bounds__(RED_THREADS)
 pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int DPL = D / 32;
-    constexpr int NB = 16;               // partials merged per batch, one per lane
+    // partials merged per batch, one per lane: 8 when a sequence has a
+    // handful (fewer registers, measured faster), 16 for partitioned
+    // sequences with hundreds
+    constexpr int NB = WPI == 1 ? 8 : 16;
     constexpr int NW = RED_THREADS / 32;
     constexpr int HPB = NW / WPI;        // heads per CTA
     static_assert(WPI == 1 || HPB == 1, "split heads take the whole CTA");
