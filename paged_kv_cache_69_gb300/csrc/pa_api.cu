@@ -191,15 +191,22 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     const bool native8 = !mq && tc && is_fp8(kv_dtype) && D == 128 && Hq / Hkv <= 8 &&
                          partition_tokens % 32 == 0;
     const bool fp8t = native8 && Hq / Hkv <= 4;      // keys as the MMA rows: half the MMAs
-    // Several query tokens with 96-128 (token, head) rows per KV head on a
-    // 16-bit cache: the tcgen05 kernel, all rows of a KV head in one 128-row
-    // tile with the accumulators in tensor memory, 32-token chunks.  (With
-    // fewer rows only some of its warps hold rows and the per-row softmax
-    // runs serially; the mma.sync kernel is faster there.)
-    const bool um = mq && !is_fp8(kv_dtype) && QL * (Hq / Hkv) >= 96 && QL * (Hq / Hkv) <= 128 &&
-                    partition_tokens % 32 == 0;
-    const int CT = (native8 || um) ? 32 : 16;
-    const void* kern = um      ? decode_kernel_mq_um(kv_dtype, q_dtype, D)
+    // Several query tokens with 48-128 (token, head) rows per KV head on a
+    // 16-bit cache: the tcgen05 kernel.  The rows of UH KV heads, each
+    // head's padded to a multiple of 32, fill a 128-row tile with the
+    // accumulators in tensor memory; a chunk is 32 tokens of its one or two
+    // heads (16-32 KB of K and V per pipeline stage).
+    const int um_rows = 32 * cdiv_h(static_cast<long long>(QL) * (Hq / Hkv), 32);
+    int UH = 0;
+    for (int h = std::min(4, 128 / std::max(1, um_rows)); h >= 1; --h)
+        if (Hkv % h == 0) { UH = h; break; }
+    const int um_ct = 32;
+    // From 48 rows up: with fewer, the per-row softmax of a 16- or 32-token
+    // chunk leaves most of the tile idle and the mma.sync kernel is faster.
+    const bool um = mq && !is_fp8(kv_dtype) && QL * (Hq / Hkv) >= 48 && um_rows <= 128 && UH > 0 &&
+                    partition_tokens % um_ct == 0;
+    const int CT = um ? um_ct : native8 ? 32 : 16;
+    const void* kern = um      ? decode_kernel_mq_um(kv_dtype, q_dtype, D, CT)
                        : mq    ? decode_kernel_mq(kv_dtype, q_dtype, D)
                        : fp8t  ? decode_kernel_fp8t(kv_dtype, q_dtype, D)
                        : native8 ? decode_kernel_e4m3(kv_dtype, q_dtype, D)
@@ -231,7 +238,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         HPC = h;
         break;
     }
-    if (um) HPC = 1;                 // one KV head per CTA: its rows fill the tile
+    if (um) HPC = UH;                // the KV heads whose row blocks fill the tile
     if (HPC == 0) return fail(PA_ERR_UNSUPPORTED, "decode: no head grouping fits one CTA");
     const int NHG = Hkv / HPC;
     // tcgen05 path: 4 consumer warps (one tile row per thread), the producer
@@ -262,17 +269,17 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     p.q_bytes = static_cast<uint32_t>(QL * HPC * G * D * eq);
     p.q_slot_bytes = (p.q_bytes + 1023u) & ~1023u;   // swizzled tensor copies need 1024-B alignment
     if (um) {
-        // column planes of the query rows 1024-B aligned.  The MMA reads 128
-        // rows from every plane; the rows past the valid ones may fall in the
-        // next plane, slot or the P buffers after the ring -- shared memory
-        // of this CTA whose values only reach tile rows that are never used.
-        p.q_plane_bytes = static_cast<uint32_t>((QL * G * 128 + 1023) & ~1023);
+        // a column plane holds the 128 tile rows (head hl's query rows at row
+        // um_rows * hl); the rows between the heads' blocks are never written
+        // and reach only tile rows nobody reads
+        p.um_rows = um_rows;
+        p.q_plane_bytes = 128u * 128u;
         p.q_slot_bytes = static_cast<uint32_t>(DH) * p.q_plane_bytes;
     }
     p.stage_bytes = 2 * p.kv_bytes;
     // CUDA-core variant: private fp32 query rows; transposed fp8: P bytes per warp
-    // tcgen05 path: two P buffers of 128 rows x 32 tokens
-    const uint32_t simtq = um ? 2u * 128u * 32u * 2u
+    // tcgen05 path: two P buffers of 128 rows x CT tokens per head
+    const uint32_t simtq = um ? 2u * static_cast<uint32_t>(HPC) * 128u * static_cast<uint32_t>(CT) * 2u
                          : fp8t ? static_cast<uint32_t>(NCW * 256) : tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
     const uint32_t extras = 1024;   // barriers, stage descriptors, prologue scratch
     const uint32_t fixed = NQ * p.q_slot_bytes + simtq + extras + 1024;   // + base alignment slack
@@ -287,7 +294,9 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     const int by_regs = std::max(1, 65536 / std::max(1, regs * threads));
     const long long sm_smem = std::min(dev.max_smem, 227 * 1024) + 1024LL;   // per-SM budget incl. reservation
     int stages = 0;
-    if (by_regs >= 2) {
+    // tcgen05 kernels run one CTA per SM (their tensor-memory allocation
+    // limits residency): size the ring for one CTA
+    if (by_regs >= 2 && !um) {
         const long long per_cta = sm_smem / 2 - 1024 - fixed;
         const int s2 = static_cast<int>(std::min<long long>(MAX_STAGES, per_cta / p.stage_bytes));
         // the multi-token query ring takes more shared memory: two stages
@@ -352,8 +361,9 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         const cuuint32_t dhq = static_cast<cuuint32_t>(D * eq / 128);
         cuuint64_t dims[4] = {e128q, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(std::max(total_q, 1)), dhq};
         cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * eq, static_cast<cuuint64_t>(Hq) * D * eq, 128};
-        // tcgen05 path: one column plane per copy
-        cuuint32_t box[4] = {e128q, static_cast<cuuint32_t>(HPC * G), static_cast<cuuint32_t>(QL), um ? 1u : dhq};
+        // tcgen05 path: one KV head's rows and one column plane per copy
+        cuuint32_t box[4] = {e128q, static_cast<cuuint32_t>(um ? G : HPC * G), static_cast<cuuint32_t>(QL),
+                             um ? 1u : dhq};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (!enc || HPC * G > 256 || QL > 256 ||
             enc(&tq, tmap_type(q_dtype), 4, const_cast<void*>(q), dims, strides, box, es,

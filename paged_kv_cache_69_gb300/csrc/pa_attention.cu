@@ -19,10 +19,12 @@ const void* decode_kernel_mq(pa_dtype kv, pa_dtype q, int D) {
     return nullptr;
 }
 
-const void* decode_kernel_mq_um(pa_dtype kv, pa_dtype q, int D) {
-#define PA_UM(KVT, DD) reinterpret_cast<const void*>(&pa_decode_kernel<KVT, KVT, DD, true, 32, true, false, true>)
-    if (kv == PA_F16 && q == PA_F16) return D == 128 ? PA_UM(F16T, 128) : D == 64 ? PA_UM(F16T, 64) : nullptr;
-    if (kv == PA_BF16 && q == PA_BF16) return D == 128 ? PA_UM(BF16T, 128) : D == 64 ? PA_UM(BF16T, 64) : nullptr;
+const void* decode_kernel_mq_um(pa_dtype kv, pa_dtype q, int D, int CT) {
+#define PA_UM(KVT, DD, C) reinterpret_cast<const void*>(&pa_decode_kernel<KVT, KVT, DD, true, C, true, false, true>)
+#define PA_UM_CT(KVT, DD) (CT == 32 ? PA_UM(KVT, DD, 32) : nullptr)
+    if (kv == PA_F16 && q == PA_F16) return D == 128 ? PA_UM_CT(F16T, 128) : D == 64 ? PA_UM_CT(F16T, 64) : nullptr;
+    if (kv == PA_BF16 && q == PA_BF16) return D == 128 ? PA_UM_CT(BF16T, 128) : D == 64 ? PA_UM_CT(BF16T, 64) : nullptr;
+#undef PA_UM_CT
 #undef PA_UM
     return nullptr;
 }

@@ -94,6 +94,7 @@ struct DecodeParams {
     int per_head_copies;      // 1: one TMA copy per (head, 128-B column block)
     int q_tma;                // 1: query rows arrive by a 128-B-swizzled tensor copy
     uint32_t q_plane_bytes;   // tcgen05 path: distance between the query slot's 128-B column planes
+    int um_rows;              // tcgen05 path: tile rows per KV head (its query rows padded to 32)
 };
 
 __device__ __forceinline__ int cdiv_i(int a, int b) { return (a + b - 1) / b; }
@@ -194,8 +195,10 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
     const int i0 = min(p.B, tid * per), i1 = min(p.B, i0 + per);
     int csum = 0, usum = 0;
     bool bad = false;
+    int L0raw = 0;                      // the first of the thread's lengths, reused below
     for (int i = i0; i < i1; ++i) {
         const int Lraw = p.seq_lens[i];
+        if (i == i0) L0raw = Lraw;
         bad |= (Lraw < 0 || Lraw > maxL);
         const int L = clamp_len(Lraw, maxL);
         csum += cdiv_i(L, p.ct);
@@ -251,7 +254,7 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
                 return first_chunk_from(t, a, base, p.WQ);
             };
             for (int i = i0; i < i1 && (need_lo || need_hi); ++i) {
-                const int L = clamp_len(p.seq_lens[i], maxL);
+                const int L = clamp_len(i == i0 ? L0raw : p.seq_lens[i], maxL);
                 const int nch = cdiv_i(L, p.ct), nu = n_units(L, p.PC, p.ct);
                 if (nch > 0) {
                     if (need_lo) {
@@ -371,12 +374,10 @@ struct DecodeKernel {
     static constexpr int KS = D / 16;         // 16-deep k-steps over head_dim
     static constexpr int ROWB = D * KV::bytes;  // bytes of one K/V row
     static constexpr int CPR = ROWB / 16;     // 16-byte chunks per row
-    static_assert(!UM || (MQ && TC && !FP8 && CT == 32), "tcgen05 path: several query tokens, 16-bit caches");
+    static_assert(!UM || (MQ && TC && !FP8), "tcgen05 path: several query tokens, 16-bit caches");
     static constexpr int UM_M = 128;          // tcgen05 tile rows: (query token, head) rows of one KV head
     static constexpr int UM_TCOLS = 256;      // tensor-memory columns per CTA: two S buffers, then O
-    static_assert(!UM || 2 * CT + D <= UM_TCOLS, "two S buffers and O fit the allocation");
-    static constexpr int UM_O = 2 * CT;       // first column of O
-    static constexpr uint32_t UM_PBUF = UM_M * CT * 2;   // bytes of one P buffer
+    static constexpr uint32_t UM_PBUF = UM_M * CT * 2;   // bytes of one P buffer (one head, one chunk)
 
     // ---------------- producer ----------------
     static __device__ void producer(const DecodeParams& p, const Plan& pl, int hg, uint8_t* base,
@@ -406,6 +407,12 @@ struct DecodeKernel {
         };
         load_lens(pl.seq);
         int i = pl.seq, Si = pl.S, Ui = pl.U;
+        int j = pl.cs - Si;
+        int wbase = (j * CT) / p.bs;                        // current window: blocks [wbase, wbase+32) of i
+        // The first window is bounded by the table row instead of the
+        // sequence's block count, so it loads alongside the lengths rather
+        // than after them (entries past the sequence are never used).
+        int wval = load_win(i, wbase, p.MB);
         int L = len_of(i);
         // first query row and query count of sequence i (one per sequence in decode)
         int qrow_i = i, qn_i = 1;
@@ -422,10 +429,7 @@ struct DecodeKernel {
         };
         load_q_rows();
         int nch = cdiv_i(L, CT), nbl = cdiv_i(L, p.bs);
-        int j = pl.cs - Si;
         const int nb = p.bs >= CT ? 1 : CT / p.bs;      // boxes per chunk
-        int wbase = (j * CT) / p.bs;                        // current window: blocks [wbase, wbase+32) of i
-        int wval = load_win(i, wbase, nbl);
         int nseq = 0, nbase = 0, nval = -1;                    // its successor
         auto prefetch_next = [&]() {
             if (wbase + 32 < nbl) {
@@ -543,12 +547,15 @@ struct DecodeKernel {
                             (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
                         uint8_t* qdst = base + p.q_off + qs * p.q_slot_bytes;
                         if constexpr (UM) {
-                            // one copy per 128-B column plane, planes q_plane_bytes
-                            // (a multiple of 1024) apart: the swizzle atoms of
-                            // every plane start aligned for the MMA descriptors
+                            // per KV head of the CTA and 128-B column plane one
+                            // copy of its [token][head] rows, to tile row
+                            // um_rows * head; planes q_plane_bytes (a multiple of
+                            // 1024) apart, so every swizzle atom starts aligned
+                            for (int hl = 0; hl < p.HPC; ++hl)
 #pragma unroll
-                            for (int dh = 0; dh < ROWB / 128; ++dh)
-                                tma_load_4d(qdst + dh * p.q_plane_bytes, tq, &full[slot], 0, hq0, qrow_i, dh);
+                                for (int dh = 0; dh < ROWB / 128; ++dh)
+                                    tma_load_4d(qdst + dh * p.q_plane_bytes + hl * p.um_rows * 128, tq, &full[slot], 0,
+                                                hq0 + hl * p.G, qrow_i, dh);
                         } else if constexpr (MQ) {
                             // rows [token][head] of QL tokens x HPC*G heads, one 4-D copy
                             tma_load_4d(qdst, tq, &full[slot], 0, hq0, qrow_i, 0);
@@ -1417,16 +1424,18 @@ struct DecodeKernel {
     }
 
     // ---------------- tcgen05 consumer (several query tokens per KV head) ----------------
-    // One KV head per CTA.  Its (query token, head) rows are the M = 128 rows
-    // of the tile: row r is tensor-memory lane r, owned by thread r of the
-    // consumer warps 0-3.  Per chunk the MMA warp computes S = Q K^T into one
+    // HPC KV heads per CTA: each head's (query token, head) rows are a block
+    // of um_rows rows (its rows padded to a multiple of 32) of the M = 128
+    // tile, so every consumer warp owns rows.  Row r is tensor-memory lane r,
+    // owned by thread r of the consumer warps 0-3.  Per chunk the MMA warp
+    // computes S = Q K^T into one
     // of two S buffers in tensor memory; each row's thread masks (sequence
     // end, causal limit), exponentiates against a reference maximum and
     // writes its weights to a K-major P buffer in shared memory (two,
     // alternating); the MMA warp then adds P V into O (M x D fp32 in tensor
     // memory) with V read in place from the stage as an MN-major operand.
-    // Chunks are 32 tokens (two 16-token MMA steps each way), so one
-    // producer iteration moves 16 KB of one head's K and V.
+    // A chunk is 32 tokens of one or two heads, so one producer iteration
+    // moves 16-32 KB of K and V.
     // The reference maximum moves only when a row's maximum passes it by more
     // than 2^8, and only then is that row of O rescaled (tcgen05.ld / st), so
     // acc, l and m of a partial all refer to it.  V rows of tokens outside the
@@ -1439,16 +1448,26 @@ struct DecodeKernel {
     static __device__ void consumer_um(const DecodeParams& p, const Plan& pl, int hg, int w, uint8_t* base,
                                        uint64_t* full, UmBars* ub, const StageDesc* descs) {
         const int lane = threadIdx.x & 31;
-        const int R = w * 32 + lane;
+        const int R = w * 32 + lane;                      // tile row = tensor-memory lane
+        const int hl = R / p.um_rows;                     // KV head of the CTA owning this row
+        const int rr = R - hl * p.um_rows;                // row within that head's block
         const int rows = p.QL * p.G;
-        const int jrow = R / p.G;                         // query token of this row
-        const int head = hg * p.G + (R - jrow * p.G);     // one KV head per CTA
+        const int jrow = rr / p.G;                        // query token of this row
+        const int head = (hg * p.HPC + hl) * p.G + (rr - jrow * p.G);
+        const bool row_in = hl < p.HPC && rr < rows;
         const uint32_t trow = ub->tmem + (static_cast<uint32_t>(w * 32) << 16);
+        const uint32_t sspan = static_cast<uint32_t>(CT * p.HPC);   // columns of one S buffer
+        const uint32_t ocol = 2u * sspan;                          // first column of O
         const int S = p.stages;
-        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u, static_cast<uint32_t>(p.rpb) * 128u,
-                           p.rpb};
+        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
+                           static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
         uint8_t* pbuf0 = base + p.simtq_off;
         constexpr uint32_t FULLM = CT == 32 ? 0xffffffffu : ((1u << CT) - 1u);
+        // P buffers start at zero: a head's buffer only ever gets its own
+        // rows, so the other heads' rows contribute nothing to its P V
+        for (uint32_t i = threadIdx.x; i < 2u * p.HPC * UM_PBUF / 16u; i += UM_M)
+            reinterpret_cast<uint4*>(pbuf0)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
         float m_ref = -INFINITY, l = 0.f;
         bool row_ok = false;
         int lim = -1;
@@ -1460,30 +1479,40 @@ struct DecodeKernel {
             uint8_t* vbuf = base + slot * p.stage_bytes + p.kv_bytes;
             if (d.flags & SEG_START) {
                 const int qn = static_cast<int>(d.flags >> QCOUNT_SHIFT);
-                row_ok = R < rows && jrow < qn;
+                row_ok = row_in && jrow < qn;
                 lim = row_ok ? d.qpos0 + jrow : -1;
                 m_ref = -INFINITY;
                 l = 0.f;
             }
             if ((d.vmask & FULLM) != FULLM) {
-                for (int i = R; i < CT * CPR; i += UM_M) {
-                    const int t = i / CPR, c = i - t * CPR;
+                // V rows of tokens outside the valid mask -> 0, every head
+                for (int i = R; i < CT * CPR * p.HPC; i += UM_M) {
+                    const int t = i / (CPR * p.HPC), r2 = i - t * (CPR * p.HPC);
+                    const int h2 = r2 / CPR, c = r2 - h2 * CPR;
                     if (!((d.vmask >> t) & 1u))
-                        *reinterpret_cast<uint4*>(vbuf + lay.chunk_addr(lay.row_base(t, 0), t, c)) =
+                        *reinterpret_cast<uint4*>(vbuf + lay.chunk_addr(lay.row_base(t, h2), t, c)) =
                             make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // ---- this row's scores of the chunk ----
+            // ---- this row's scores: token t of the chunk sits in column
+            // (t / rpb) * HPC * rpb + head * rpb + t % rpb of the S buffer ----
             if (!(ok = warp_wait(&ub->sfull[st & 1], (st >> 1) & 1u))) break;
             tc05_fence_after();
             float s[CT];
             {
-                float h0[16], h1[16];
-                tmem_ld16(trow + (st & 1) * CT, h0);
-                tmem_ld16(trow + (st & 1) * CT + 16, h1);
-                tmem_wait_ld();
+                const uint32_t sb = trow + (st & 1) * sspan;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) { s[t] = h0[t]; s[16 + t] = h1[t]; }
+                for (int b8 = 0; b8 < CT / 8; ++b8) {
+                    const int t0 = 8 * b8;
+                    const int bx = t0 / p.rpb;
+                    const uint32_t col = static_cast<uint32_t>((bx * p.HPC + (hl < p.HPC ? hl : 0)) * p.rpb +
+                                                               (t0 - bx * p.rpb));
+                    float v8[8];
+                    tmem_ld8(sb + col, v8);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s[t0 + i] = v8[i];
+                }
+                tmem_wait_ld();
             }
             float alpha = 1.f;
             bool resc = false;
@@ -1514,7 +1543,7 @@ struct DecodeKernel {
 #pragma unroll
                 for (int t = 0; t < CT; ++t) s[t] = 0.f;
             }
-            // P buffer st % 2 is free once P V of chunk st - 2 is complete
+            // P buffers st % 2 are free once P V of chunk st - 2 is complete
             if (st >= 2 && !(ok = warp_wait(&ub->pvdone[st & 1], ((st >> 1) - 1) & 1u))) break;
             if (__any_sync(0xffffffffu, resc)) {
                 // rescale this warp's rows of O: P V of chunk st - 1 must be complete
@@ -1523,22 +1552,24 @@ struct DecodeKernel {
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 16) {
                     float o[16];
-                    tmem_ld16(trow + UM_O + c0, o);
+                    tmem_ld16(trow + ocol + c0, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) o[i] *= alpha;
-                    tmem_st16(trow + UM_O + c0, o);
+                    tmem_st16(trow + ocol + c0, o);
                 }
                 tmem_wait_st();
             }
-            // ---- P: row R as CT / 8 core-matrix rows of 8 tokens (16 bytes each) ----
-            uint8_t* pb = pbuf0 + (st & 1) * UM_PBUF;
+            // ---- P: row R of its head's buffer, CT / 8 core-matrix rows of 8 tokens ----
+            if (row_in) {
+                uint8_t* pb = pbuf0 + ((st & 1) * p.HPC + hl) * UM_PBUF;
 #pragma unroll
-            for (int kc = 0; kc < CT / 8; ++kc) {
-                const float* w = s + 8 * kc;
-                *reinterpret_cast<uint4*>(pb + (kc * (UM_M / 8) + (R >> 3)) * 128 + (R & 7) * 16) =
-                    make_uint4(pack2(w[0], w[1], MMA_BF16), pack2(w[2], w[3], MMA_BF16),
-                               pack2(w[4], w[5], MMA_BF16), pack2(w[6], w[7], MMA_BF16));
+                for (int kc = 0; kc < CT / 8; ++kc) {
+                    const float* v = s + 8 * kc;
+                    *reinterpret_cast<uint4*>(pb + (kc * (UM_M / 8) + (R >> 3)) * 128 + (R & 7) * 16) =
+                        make_uint4(pack2(v[0], v[1], MMA_BF16), pack2(v[2], v[3], MMA_BF16),
+                                   pack2(v[4], v[5], MMA_BF16), pack2(v[6], v[7], MMA_BF16));
+                }
             }
             fence_proxy_async_smem();            // P and zeroed V rows visible to the tensor core
             tc05_fence_before();
@@ -1547,7 +1578,7 @@ struct DecodeKernel {
             if (d.flags & SEG_END) {
                 if (!(ok = warp_wait(&ub->pvdone[st & 1], (st >> 1) & 1u))) break;
                 tc05_fence_after();
-                finish_segment_um(p, d, trow, row_ok, jrow, head, m_ref, l);
+                finish_segment_um(p, d, trow + ocol, row_ok, jrow, head, m_ref, l);
                 tc05_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ub->ofree);
@@ -1556,10 +1587,10 @@ struct DecodeKernel {
         if (!ok && lane == 0) raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
     }
 
-    // End of a segment on the tcgen05 path: this thread's row of O, normalised
-    // into the output when the segment covers the whole sequence, else the
-    // unnormalised partial (acc, m, l).
-    static __device__ __forceinline__ void finish_segment_um(const DecodeParams& p, const StageDesc& d, uint32_t trow,
+    // End of a segment on the tcgen05 path: this thread's row of O (tensor
+    // memory at `orow`), normalised into the output when the segment covers
+    // the whole sequence, else the unnormalised partial (acc, m, l).
+    static __device__ __forceinline__ void finish_segment_um(const DecodeParams& p, const StageDesc& d, uint32_t orow_t,
                                                              bool row_ok, int jrow, int head, float m, float l) {
         const bool direct = (d.flags & DIRECT) != 0;
         const bool store = row_ok && (direct || d.slot < p.max_slots);
@@ -1570,7 +1601,7 @@ struct DecodeKernel {
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
             float o[16];
-            tmem_ld16(trow + UM_O + c0, o);
+            tmem_ld16(orow_t + c0, o);
             tmem_wait_ld();
             if (store) {
 #pragma unroll
@@ -1603,21 +1634,32 @@ struct DecodeKernel {
     // of chunk st when its bytes have landed, so the scores of the next chunk
     // are ready when the consumers finish the current one; otherwise P V of
     // chunk st goes first and frees its stage without waiting for memory.
+    //   S: with several KV heads per CTA one MMA per box of rpb tokens and
+    //   K-step takes the box's rows of every head (N = HPC * rpb, rows 128 B
+    //   apart); the products of one head's query rows with another head's keys
+    //   land in columns nobody reads.  With one head, one MMA per 16 tokens.
+    //   P V: per head, P of that head (its rows only, the rest zero) times
+    //   its V, 16 tokens per MMA.
     static __device__ void mma_um(const DecodeParams& p, const Plan& pl, uint8_t* base, uint64_t* full,
                                   uint64_t* empty, uint64_t* qempty, UmBars* ub, const StageDesc* descs) {
         const int S = p.stages;
+        const int HPC = p.HPC;
         const uint32_t tm = ub->tmem;
-        const uint32_t id_s = umma_idesc_f16(MMA_BF16, UM_M, 16, false, false);
+        const uint32_t sspan = static_cast<uint32_t>(CT * HPC);
+        const uint32_t ocol = 2u * sspan;
+        const int nbox = CT / p.rpb;                      // TMA boxes per chunk
+        const bool multi = HPC > 1;
+        const uint32_t id_s = umma_idesc_f16(MMA_BF16, UM_M, multi ? HPC * p.rpb : 16, false, false);
         const uint32_t id_o = umma_idesc_f16(MMA_BF16, UM_M, D, false, true);
-        // K and V of a stage: 8-token groups 1024 B apart inside a box of 16
-        // or more rows, one box apart with 8-row boxes; 64-element column
-        // blocks rpb * 128 B apart (one head per CTA)
+        // 8-token groups of one head's K / V rows: 1024 B apart inside a box
+        // of 16 or more rows, one box apart with 8-row boxes; 64-element
+        // column blocks HPC * rpb * 128 B apart
         const uint32_t grp = p.rpb == 8 ? p.box_bytes : 1024u;
-        const uint32_t dhs = static_cast<uint32_t>(p.rpb) * 128u;
+        const uint32_t dhs = static_cast<uint32_t>(HPC * p.rpb) * 128u;
         const uint32_t pb0 = smem_u32(base + p.simtq_off);
-        // byte offset of token t0 (a multiple of 8) in a stage's K or V buffer
-        auto tok_off = [&](int t0) -> uint32_t {
-            return static_cast<uint32_t>(t0 / p.rpb) * p.box_bytes + static_cast<uint32_t>(t0 % p.rpb) * 128u;
+        // byte offset of head h's token t0 (a multiple of 8) in a stage's K or V buffer
+        auto tok_off = [&](int t0, int h) -> uint32_t {
+            return static_cast<uint32_t>(t0 / p.rpb) * p.box_bytes + static_cast<uint32_t>(h * p.rpb + t0 % p.rpb) * 128u;
         };
         bool ok = true;
         int q_cur = 0;          // query ring slot of the current segment (descriptors name it at its first chunk)
@@ -1628,16 +1670,18 @@ struct DecodeKernel {
             if (d.flags & SEG_START) q_cur = d.qslot;
             const uint32_t qb = smem_u32(base + p.q_off + q_cur * p.q_slot_bytes);
             const uint32_t kb = smem_u32(base + slot * p.stage_bytes);
-            // S for tokens 16h .. 16h + 15 into columns 16h .. of the buffer
-#pragma unroll
-            for (int h = 0; h < CT / 16; ++h) {
-                const uint32_t kh = kb + tok_off(16 * h);
+            const uint32_t sb = tm + (st & 1) * sspan;
+            const int nmma = multi ? nbox : CT / 16;
+            for (int m = 0; m < nmma; ++m) {
+                // multi: box m, all heads (columns m * HPC * rpb ..); else tokens 16m .. 16m + 15
+                const uint32_t kbase = multi ? kb + static_cast<uint32_t>(m) * p.box_bytes : kb + tok_off(16 * m, 0);
+                const uint32_t dcol = multi ? static_cast<uint32_t>(m * HPC * p.rpb) : static_cast<uint32_t>(16 * m);
+                const uint32_t ksbo = multi ? 1024u : grp;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t plane = static_cast<uint32_t>(kk >> 2), within = static_cast<uint32_t>(kk & 3) * 32u;
-                    umma_f16(tm + (st & 1) * CT + 16 * h,
-                             umma_desc(qb + plane * p.q_plane_bytes + within, 16u, 1024u, 2u),
-                             umma_desc(kh + plane * dhs + within, 16u, grp, 2u), id_s, kk > 0);
+                    umma_f16(sb + dcol, umma_desc(qb + plane * p.q_plane_bytes + within, 16u, 1024u, 2u),
+                             umma_desc(kbase + plane * dhs + within, 16u, ksbo, 2u), id_s, kk > 0);
                 }
             }
             umma_commit(&ub->sfull[st & 1]);
@@ -1670,12 +1714,14 @@ struct DecodeKernel {
             if (first) ++seg;
             tc05_fence_after();
             const uint32_t vb = smem_u32(base + slot * p.stage_bytes + p.kv_bytes);
-            // O += P V, one 16-token K step at a time
+            for (int h = 0; h < HPC; ++h) {
+                const uint32_t pbh = pb0 + static_cast<uint32_t>((st & 1) * HPC + h) * UM_PBUF;
 #pragma unroll
-            for (int h = 0; h < CT / 16; ++h)
-                umma_f16(tm + UM_O,
-                         umma_desc(pb0 + (st & 1) * UM_PBUF + h * 2u * (UM_M / 8) * 128u, (UM_M / 8) * 128u, 128u, 0u),
-                         umma_desc(vb + tok_off(16 * h), dhs, grp, 2u), id_o, !first || h > 0);
+                for (int k16 = 0; k16 < CT / 16; ++k16)
+                    umma_f16(tm + ocol,
+                             umma_desc(pbh + k16 * 2u * (UM_M / 8) * 128u, (UM_M / 8) * 128u, 128u, 0u),
+                             umma_desc(vb + tok_off(16 * k16, h), dhs, grp, 2u), id_o, !first || h > 0 || k16 > 0);
+            }
             umma_commit(&ub->pvdone[st & 1]);
             umma_commit(&empty[slot]);                                 // K and V of the stage are read
             if (!s_next && !(ok = issue_s(st + 1))) break;

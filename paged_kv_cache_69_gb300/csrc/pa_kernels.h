@@ -14,8 +14,9 @@ const void* decode_kernel_fp8t(pa_dtype kv, pa_dtype q, int D);
 // several (causal) query tokens per sequence, tensor cores.
 const void* decode_kernel_mq(pa_dtype kv, pa_dtype q, int D);
 // the same on the 5th-generation tensor cores (tcgen05, accumulators in
-// tensor memory), 16-bit caches, more than 16 (token, head) rows per KV head.
-const void* decode_kernel_mq_um(pa_dtype kv, pa_dtype q, int D);
+// tensor memory), 16-bit caches, more than 16 (token, head) rows per KV
+// head; chunks of CT = 32 tokens.
+const void* decode_kernel_mq_um(pa_dtype kv, pa_dtype q, int D, int CT);
 // Log-sum-exp merge; split_heads: several warps per (sequence, head), for
 // partitioned sequences with many partials.
 const void* reduce_kernel(pa_dtype out, int D, bool split_heads);

@@ -1,5 +1,7 @@
 """GPU parity of pa_attention (several causal query tokens per sequence)
-against the oracle, through the C interface."""
+against the oracle, through the C interface.  Shapes with 48-128 (token,
+head) rows per KV head on 16-bit caches run the tcgen05 kernel (the 56- and
+128-row families below), the others the mma.sync kernel."""
 import numpy as np
 import pytest
 import torch
@@ -54,6 +56,8 @@ MQ_CASES = [
     ("f16", None, 128, 16, 64, 4, [80, 600], [8, 2], 0),                     # 128 rows: 8 tiles
     ("bf16", None, 128, 8, 32, 8, [7, 200, 999], [4, 8, 2], 64),             # bs 8: two boxes per chunk
     ("f16", None, 128, 64, 28, 4, [10, 64, 65, 700], [3, 8, 1, 8], 0),      # bs 64: chunks inside a block
+    ("bf16", None, 128, 8, 28, 4, [7, 200, 999], [8, 8, 2], 64),            # 56 rows, bs 8: 8-row boxes
+    ("f16", None, 128, 32, 28, 4, [40, 500, 33], [7, 8, 8], 0),              # 56 rows, bs 32: 32-row boxes
     ("fp8_e4m3", "bf16", 128, 32, 32, 8, [90, 3000], [3, 6], 0),
     ("fp8_e5m2", "f16", 128, 16, 28, 4, [50, 900], [2, 4], 0),
 ]
