@@ -417,11 +417,12 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     if (ce != cudaSuccess) return fail_cuda("decode: main kernel launch", ce);
 
     cudaLaunchConfig_t rcfg{};
+    const int red_block = red_threads(split_heads ? RED_SPLIT_WARPS : 1);
     {
         // persistent reduce grid: one wave of CTAs striding over the
         // (split sequence, head group) items
         int red_per_sm = 0;
-        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&red_per_sm, rkern, RED_THREADS, 0);
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&red_per_sm, rkern, red_block, 0);
         if (ce != cudaSuccess) return fail_cuda("decode: reduce occupancy query", ce);
         const long long items = static_cast<long long>(QL) *
                                 (split_heads ? static_cast<long long>(B) * Hq
@@ -429,7 +430,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
         const long long g = std::max(1LL, std::min(items, static_cast<long long>(std::max(1, red_per_sm)) * dev.sms));
         rcfg.gridDim = dim3(static_cast<unsigned>(g));
     }
-    rcfg.blockDim = dim3(RED_THREADS);
+    rcfg.blockDim = dim3(static_cast<unsigned>(red_block));
     rcfg.dynamicSmemBytes = 0;
     rcfg.stream = stream;
     rcfg.attrs = attr;

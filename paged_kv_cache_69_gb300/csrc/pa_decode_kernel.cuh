@@ -44,7 +44,11 @@ constexpr int MAX_WARPS = 9;         // up to 8 consumers + 1 producer
 // its sequence continues in the next range; the slot after the segment's
 // would stay unwritten, so the segment also writes an empty partial there
 // (m = -inf, l = 0, acc = 0), keeping every sequence's partials consecutive.
-enum : uint32_t { SEG_START = 1u, SEG_END = 2u, DIRECT = 4u, GAP = 8u };
+// QLOAD: the segment's query rows were copied into ring slot qslot with this
+// chunk.  A partition start inside a sequence that the CTA has already begun
+// keeps the query fragments the consumers hold (the tcgen05 path, which reads
+// the query from shared memory, always copies).
+enum : uint32_t { SEG_START = 1u, SEG_END = 2u, DIRECT = 4u, GAP = 8u, QLOAD = 16u };
 
 struct StageDesc {
     int seq;
@@ -440,14 +444,24 @@ struct DecodeKernel {
         };
         prefetch_next();
         const int hq0 = hg * p.HPC * p.G;
+        const int range = blockIdx.x / p.NHG;
         int issued = 0, qcount = 0;
+        int slot = 0, qs = 0;                 // issued % S, qcount % NQ
+        uint32_t round = 0, qround = 0;       // issued / S, qcount / NQ
+        // Chunk j of sequence i is chunk jp of its partition ju (jp = j and
+        // ju = 0 without partitions), tracked incrementally: a division by
+        // the partition length per chunk, on the path from a stage coming
+        // free to its refill, cost 7-10% with 512-token partitions.
+        int jp = j, ju = 0;
+        if (p.PC > 0) { ju = j / p.PC; jp = j - ju * p.PC; }
         bool ok = true;
         for (int k = pl.cs; k < pl.ce; ++k) {
             while (j >= nch) {
                 Si += nch; Ui += n_units(L, p.PC, p.ct); ++i;
                 L = len_of(i);
                 load_q_rows();
-                nch = cdiv_i(L, CT); nbl = cdiv_i(L, p.bs); j = 0;
+                nch = cdiv_i(L, CT); nbl = cdiv_i(L, p.bs);
+                j = 0; jp = 0; ju = 0;
                 wbase = 0;
                 wval = (nseq == i && nbase == 0) ? nval : load_win(i, 0, nbl);
                 prefetch_next();
@@ -466,60 +480,57 @@ struct DecodeKernel {
 #pragma unroll
             for (int b = 0; b < MAXB; ++b) blk[b] = __shfl_sync(0xffffffffu, wval, min(b0 + b - wbase, 31));
             if (lane == 0) {
-                const int slot = issued % S;
-                const uint32_t round = issued / S;
                 if (issued >= S && !mbar_wait_bounded(&empty[slot], (round - 1) & 1u)) {
                     raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
                     ok = false;
                 }
-                const bool seg_start = (k == pl.cs) || (j == 0) || (p.PC > 0 && j % p.PC == 0);
-                const int qs = qcount % NQ;
-                if (ok && seg_start && qcount >= NQ &&
-                    !mbar_wait_bounded(&qempty[qs], ((qcount / NQ) - 1) & 1u)) {
+                const bool seg_start = (k == pl.cs) || (jp == 0);
+                const bool qload = seg_start && (UM || k == pl.cs || j == 0);
+                const int ntok = min(CT, L - tok0);
+                const uint32_t vmask_full = CT == 32 ? 0xffffffffu : ((1u << CT) - 1u);
+                uint32_t vmask = (ntok >= 32) ? 0xffffffffu : ((1u << ntok) - 1u);
+                vmask &= vmask_full;
+                uint32_t nbox_issued = 0;
+                uint32_t issue_mask = 0;
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b) {
+                    if (b >= nb) break;
+                    const int first = b * p.rpb;
+                    if (first >= ntok) continue;                 // nothing valid here
+                    const int id = blk[b];
+                    const uint32_t rows = (p.rpb >= 32 ? 0xffffffffu : ((1u << p.rpb) - 1u)) << first;
+                    if (id < 0 || id >= p.NB) {
+                        raise_flag(p.err_flag, PA_ERRBIT_BAD_BLOCK);
+                        vmask &= ~rows;
+                        continue;
+                    }
+                    issue_mask |= 1u << b;
+                    ++nbox_issued;
+                }
+                const bool part_end = p.PC > 0 && jp == p.PC - 1;
+                uint32_t flags = 0;
+                if (seg_start) flags |= SEG_START;
+                if (qload) flags |= QLOAD;
+                if (k == pl.ce - 1 || j == nch - 1 || part_end) flags |= SEG_END;
+                if (k == pl.ce - 1 && part_end && j + 1 < nch) flags |= GAP;
+                const int nu = n_units(L, p.PC, p.ct);
+                if (nu == 1 && Si >= pl.cs && Si + nch <= pl.ce) flags |= DIRECT;
+                StageDesc d;
+                d.seq = i; d.tok0 = tok0; d.vmask = vmask;
+                d.flags = flags | (static_cast<uint32_t>(qn_i) << QCOUNT_SHIFT);
+                d.slot = range + Ui + ju;
+                d.qslot = qload ? qs : (qs == 0 ? NQ - 1 : qs - 1);
+                d.qrow0 = qrow_i;
+                d.qpos0 = L - qn_i;
+                const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (qload ? p.q_bytes : 0u);
+                if (ok && qload && qcount >= NQ && !mbar_wait_bounded(&qempty[qs], (qround - 1) & 1u)) {
                     raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
                     ok = false;
                 }
                 if (ok) {
-                    const int ntok = min(CT, L - tok0);
-                    const uint32_t vmask_full = CT == 32 ? 0xffffffffu : ((1u << CT) - 1u);
-                    uint32_t vmask = (ntok >= 32) ? 0xffffffffu : ((1u << ntok) - 1u);
-                    vmask &= vmask_full;
-                    uint32_t nbox_issued = 0;
                     uint8_t* kbuf = base + slot * p.stage_bytes;
                     uint8_t* vbuf = kbuf + p.kv_bytes;
-                    uint32_t issue_mask = 0;
-#pragma unroll
-                    for (int b = 0; b < MAXB; ++b) {
-                        if (b >= nb) break;
-                        const int first = b * p.rpb;
-                        if (first >= ntok) continue;                 // nothing valid here
-                        const int id = blk[b];
-                        const uint32_t rows = (p.rpb >= 32 ? 0xffffffffu : ((1u << p.rpb) - 1u)) << first;
-                        if (id < 0 || id >= p.NB) {
-                            raise_flag(p.err_flag, PA_ERRBIT_BAD_BLOCK);
-                            vmask &= ~rows;
-                            continue;
-                        }
-                        issue_mask |= 1u << b;
-                        ++nbox_issued;
-                    }
-                    uint32_t flags = 0;
-                    const bool seg_end = (k == pl.ce - 1) || (j == nch - 1) ||
-                                         (p.PC > 0 && (j + 1) % p.PC == 0);
-                    if (seg_start) flags |= SEG_START;
-                    if (seg_end) flags |= SEG_END;
-                    if (k == pl.ce - 1 && p.PC > 0 && (j + 1) % p.PC == 0 && j + 1 < nch) flags |= GAP;
-                    const int nu = n_units(L, p.PC, p.ct);
-                    if (nu == 1 && Si >= pl.cs && Si + nch <= pl.ce) flags |= DIRECT;
-                    StageDesc d;
-                    d.seq = i; d.tok0 = tok0; d.vmask = vmask;
-                    d.flags = flags | (static_cast<uint32_t>(qn_i) << QCOUNT_SHIFT);
-                    d.slot = (blockIdx.x / p.NHG) + Ui + (p.PC > 0 ? j / p.PC : 0);
-                    d.qslot = qs;
-                    d.qrow0 = qrow_i;
-                    d.qpos0 = L - qn_i;
                     descs[slot] = d;
-                    const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (seg_start ? p.q_bytes : 0u);
                     mbar_arrive_expect_tx(&full[slot], bytes);
 #pragma unroll
                     for (int b = 0; b < MAXB; ++b) {
@@ -542,7 +553,7 @@ struct DecodeKernel {
                                 }
                         }
                     }
-                    if (seg_start) {
+                    if (qload) {
                         const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
                             (static_cast<size_t>(i) * p.Hq + hq0) * D * QT::bytes;
                         uint8_t* qdst = base + p.q_off + qs * p.q_slot_bytes;
@@ -564,13 +575,16 @@ struct DecodeKernel {
                             else bulk_load(qdst, qsrc, p.q_bytes, &full[slot]);
                         }
                         ++qcount;
+                        if (++qs == NQ) { qs = 0; ++qround; }
                     }
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ++issued;
+            if (++slot == S) { slot = 0; ++round; }
             ++j;
+            if (++jp == p.PC) { jp = 0; ++ju; }
         }
         // drain: every copy this CTA issued must land before the CTA exits
         if (lane == 0) {
@@ -752,9 +766,11 @@ struct DecodeKernel {
             uint8_t* kbuf = base + slot * p.stage_bytes;
             uint8_t* vbuf = kbuf + p.kv_bytes;
             if (d.flags & SEG_START) {
-                load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, p, hl, mt, rows_valid, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                if (d.flags & QLOAD) {
+                    load_q_frags(qa, base + p.q_off + d.qslot * p.q_slot_bytes, p, hl, mt, rows_valid, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
                 m0 = m1 = -INFINITY; l0 = l1 = 0.f;
@@ -954,10 +970,12 @@ struct DecodeKernel {
             uint8_t* kbuf = base + slot * p.stage_bytes;
             uint8_t* vbuf = kbuf + p.kv_bytes;
             if (d.flags & SEG_START) {
-                qk_scale = p.qk_scale * load_q_e4m3(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo,
-                                                    rows_valid, lane, p.q_tma, p.HPC * p.G);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                if (d.flags & QLOAD) {
+                    qk_scale = p.qk_scale * load_q_e4m3(qa, base + p.q_off + d.qslot * p.q_slot_bytes, qrow_lo,
+                                                        rows_valid, lane, p.q_tma, p.HPC * p.G);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
                 m0 = -INFINITY; l0 = 0.f;
@@ -1111,10 +1129,12 @@ struct DecodeKernel {
             uint8_t* kbuf = base + slot * p.stage_bytes;
             uint8_t* vbuf = kbuf + p.kv_bytes;
             if (d.flags & SEG_START) {
-                qk_scale = p.qk_scale * load_q_fp8t(qb, base + p.q_off + d.qslot * p.q_slot_bytes, hl * p.G,
-                                                     p.G, lane, p.q_tma, p.HPC * p.G);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                if (d.flags & QLOAD) {
+                    qk_scale = p.qk_scale * load_q_fp8t(qb, base + p.q_off + d.qslot * p.q_slot_bytes, hl * p.G,
+                                                         p.G, lane, p.q_tma, p.HPC * p.G);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                }
 #pragma unroll
                 for (int c = 0; c < 8; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
                 m = -INFINITY; l = 0.f;
@@ -1765,11 +1785,13 @@ struct DecodeKernel {
             const uint8_t* kbuf = base + slot * p.stage_bytes;
             const uint8_t* vbuf = kbuf + p.kv_bytes;
             if (d.flags & SEG_START) {
-                const QE* qbuf = reinterpret_cast<const QE*>(base + p.q_off + d.qslot * p.q_slot_bytes);
-                for (int e = lane; e < nr * D; e += 32)
-                    qp[e] = to_float(qbuf[static_cast<size_t>(qrow_lo) * D + e]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                if (d.flags & QLOAD) {
+                    const QE* qbuf = reinterpret_cast<const QE*>(base + p.q_off + d.qslot * p.q_slot_bytes);
+                    for (int e = lane; e < nr * D; e += 32)
+                        qp[e] = to_float(qbuf[static_cast<size_t>(qrow_lo) * D + e]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&qempty[d.qslot]);
+                }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     m[r] = -INFINITY; l[r] = 0.f;
@@ -2048,22 +2070,27 @@ __device__ __forceinline__ float2 ldg_f2(const float2* p) {
 }
 
 constexpr int RED_THREADS = 128;     // 4 warps: one query head each
+constexpr int RED_SPLIT_WARPS = 16;  // warps sharing one head's partials
+
+// Threads of a merge CTA with WPI warps per (sequence, head).
+__host__ __device__ constexpr int red_threads(int wpi) { return wpi == 1 ? RED_THREADS : 32 * wpi; }
 
 // WPI warps per (sequence, head): 1 when sequences have a handful of
-// partials (each warp of the CTA takes one head), RED_THREADS / 32 when
+// partials (each warp of a 4-warp CTA takes one head), RED_SPLIT_WARPS when
 // partitioned sequences have hundreds (the CTA's warps split one head's
-// partials and combine their results through shared memory).
+// partials, so that a long sequence's reads are spread over 16 warps, and
+// combine their results through shared memory).
 template <typename OutT, int D, int WPI>
-__global__ void __launch_bounds__(RED_THREADS)
+__global__ void __launch_bounds__(red_threads(WPI))
 pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int DPL = D / 32;
-    // partials merged per batch, one per lane: 8 when a sequence has a
-    // handful (fewer registers, measured faster), 16 for partitioned
-    // sequences with hundreds
-    constexpr int NB = WPI == 1 ? 8 : 16;
-    constexpr int NW = RED_THREADS / 32;
+    // partials merged per batch, one per lane (8: fewer registers than 16,
+    // measured faster whether a warp merges a handful or a share of hundreds)
+    constexpr int NB = 8;
+    constexpr int NW = red_threads(WPI) / 32;
     constexpr int HPB = NW / WPI;        // heads per CTA
     static_assert(WPI == 1 || HPB == 1, "split heads take the whole CTA");
+    static_assert((WPI & (WPI - 1)) == 0, "the combine tree halves the warps");
     __shared__ float comb[WPI > 1 ? NW * 32 * (DPL + 2) : 1];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = warp % WPI;
@@ -2162,14 +2189,19 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
             if (cnt % NB) merge(cnt % NB, my_slot);
         }
         if constexpr (WPI > 1) {
+            // pairwise tree: at stride s, warp w (a multiple of 2s) folds in
+            // the running result of warp w + s
             float* mine = comb + (warp * 32 + lane) * (DPL + 2);
-            mine[0] = M; mine[1] = den;
 #pragma unroll
-            for (int c = 0; c < DPL; ++c) mine[2 + c] = num[c];
-            __syncthreads();
-            if (sub == 0) {
-                for (int w2 = 1; w2 < WPI; ++w2) {
-                    const float* o2 = comb + ((warp + w2) * 32 + lane) * (DPL + 2);
+            for (int s = WPI / 2; s >= 1; s >>= 1) {
+                if (sub >= s && sub < 2 * s) {
+                    mine[0] = M; mine[1] = den;
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) mine[2 + c] = num[c];
+                }
+                __syncthreads();
+                if (sub < s) {
+                    const float* o2 = comb + ((warp + s) * 32 + lane) * (DPL + 2);
                     const float M2 = o2[0];
                     const float Mn = fmaxf(M, M2);
                     const float Mu = (Mn == -INFINITY) ? 0.f : Mn;
@@ -2179,8 +2211,8 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
                     for (int c = 0; c < DPL; ++c) num[c] = num[c] * s1 + o2[2 + c] * s2;
                     M = Mn;
                 }
+                __syncthreads();              // the buffer is reused by the next stride / item
             }
-            __syncthreads();                  // the buffer is reused by the next item
             if (sub != 0) continue;
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;

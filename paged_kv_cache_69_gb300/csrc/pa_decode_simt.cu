@@ -29,9 +29,9 @@ const void* decode_kernel_simt(pa_dtype kv, pa_dtype q, int D) {
 
 const void* reduce_kernel(pa_dtype out, int D, bool split_heads) {
 #define PA_RED(T) \
-    if (D == 128) return split_heads ? reinterpret_cast<const void*>(&pa_reduce_kernel<T, 128, RED_THREADS / 32>) \
+    if (D == 128) return split_heads ? reinterpret_cast<const void*>(&pa_reduce_kernel<T, 128, RED_SPLIT_WARPS>) \
                                      : reinterpret_cast<const void*>(&pa_reduce_kernel<T, 128, 1>);          \
-    if (D == 64) return split_heads ? reinterpret_cast<const void*>(&pa_reduce_kernel<T, 64, RED_THREADS / 32>)  \
+    if (D == 64) return split_heads ? reinterpret_cast<const void*>(&pa_reduce_kernel<T, 64, RED_SPLIT_WARPS>)  \
                                     : reinterpret_cast<const void*>(&pa_reduce_kernel<T, 64, 1>);            \
     return nullptr;
     if (out == PA_F32) { PA_RED(float) }
