@@ -309,6 +309,7 @@ __device__ inline void make_plan(const DecodeParams& p, int range, int2* scratch
             U += nu;
         }
         if (tid == 0) { p.totals[0] = C; p.totals[1] = Ut; }
+        __threadfence();             // the merge kernel reads the list before this grid ends
     }
     __syncthreads();
     const int4 f = *s_first;
@@ -1963,15 +1964,16 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     // kernel on the stream (typically the cache write): its CTAs may be
     // resident before that grid ends, and wait here until it has completed
     // and its writes are visible.  The merge kernel is in turn launched as a
-    // programmatic dependent of this one and waits for this grid to
-    // complete: letting it become resident now takes its launch off the
-    // critical path.
+    // programmatic dependent of this one once every CTA has passed the
+    // trigger below: it becomes resident early, reads the merge list (made
+    // visible by CTA 0 before its trigger) and then waits for this grid to
+    // complete before reading partials.
     grid_dependency_wait();
-    grid_dependents_launch();
     const int hg = blockIdx.x % p.NHG;
     const int range = blockIdx.x / p.NHG;
     Plan pl;
     make_plan(p, range, scratch, s_first, s_tot, s_end, pl);
+    grid_dependents_launch();
     if (pl.cs >= pl.ce || pl.seq < 0) return;
 
     const int warp = threadIdx.x >> 5;
@@ -2096,11 +2098,18 @@ pa_reduce_kernel(const __grid_constant__ DecodeParams p) {
     const int sub = warp % WPI;
     const int HG = cdiv_i(p.Hq, HPB);    // head groups of HPB heads
     const int per_seq = p.QL * HG;       // items of one split sequence: query tokens x head groups
+    // The list and its length are final once every CTA of the main grid has
+    // passed its trigger, which precedes this grid's start: the first item's
+    // entry loads before the wait for the partials.
+    int count = *reinterpret_cast<volatile int*>(&p.totals[2]);
+    int4 e = __ldcg(&p.split_list[min(static_cast<int>(blockIdx.x) / per_seq, p.B - 1)]);
     grid_dependency_wait();
     for (int item = blockIdx.x;; item += gridDim.x) {
-        // the count and this item's list entry load together
-        const int count = *reinterpret_cast<volatile int*>(&p.totals[2]);
-        const int4 e = p.split_list[min(item / per_seq, p.B - 1)];
+        if (item != static_cast<int>(blockIdx.x)) {
+            // the count and this item's list entry load together
+            count = *reinterpret_cast<volatile int*>(&p.totals[2]);
+            e = __ldcg(&p.split_list[min(item / per_seq, p.B - 1)]);
+        }
         if (item >= count * per_seq) break;
         const int jq = (item / HG) % p.QL;                // query token of the sequence
         const int h = (item % HG) * HPB + warp / WPI;
