@@ -92,10 +92,16 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary of this
-    workload, when it was taken from the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"pa_decode_{workload}.md")
+def profile_name(workload: str, partition_tokens: int = 0, q_per_seq: int = 1) -> str:
+    """File stem of the committed ncu summary of one bench configuration."""
+    stem = f"pa_attention_{workload}_q{q_per_seq}" if q_per_seq > 1 else f"pa_decode_{workload}"
+    return stem + (f"_p{partition_tokens}" if partition_tokens else "")
+
+
+def profile_traffic(name: str):
+    """DRAM bytes per decode launch from the committed ncu summary `name`,
+    when it was taken from the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -504,7 +510,8 @@ def run_ours(args, rank, world, local) -> dict | None:
                         "kernel": "pa_decode (main + reduce)" if NQ == 1 else "pa_attention (main + reduce)",
                         "algorithmic_bytes_per_launch": alg,
                         "launch_ms": dec_ms, "launch_ms_stat": f"median of {n_eager} eager calls",
-                        "traffic": profile_traffic(args.workload) if NQ == 1 and not args.partition_tokens else None},
+                        "traffic": profile_traffic(profile_name(args.workload, args.partition_tokens, NQ)),
+                        "profile": f"profiles/{profile_name(args.workload, args.partition_tokens, NQ)}.md"},
            "gpu_launches": K * (3 + (1 if pairs is not None else 0)),
            "clocks": clk, "e2e": e2e,
            "cache_write_us_per_step": write_us,
@@ -623,14 +630,22 @@ def run_block_copy(args) -> dict:
     flat_h = torch.empty(moved // 2, dtype=torch.float16).pin_memory()
     t_flat_out = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), 20)
     t_flat_in = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), 20)
-    # all-layer copy-on-write: 96 pairs (the prefix-sharing COW step) in 28 layers
-    L, NB2, pairs_n = 28, 4096, 96
+    del dk, dv, hk, hv, flat_d, flat_h
+    torch.cuda.empty_cache()
+    # all-layer copy-on-write: 96 pairs (the prefix-sharing COW step) in 28
+    # layers of 2048-block pools (1.8 GB on the device)
+    L, NB2, pairs_n = 28, 2048, 96
     ks = [torch.randn(NB2, bs, Hkv, D, device=dev, dtype=torch.float16) for _ in range(L)]
     vs = [torch.randn(NB2, bs, Hkv, D, device=dev, dtype=torch.float16) for _ in range(L)]
     perm = torch.randperm(NB2, generator=g)
     cow = torch.stack([perm[:pairs_n], perm[pairs_n:2 * pairs_n]], 1).to(dev)
     t_cow = timed(lambda: pa.pa_copy_blocks_layers(ks, vs, cow), 50)
     cow_bytes = L * pairs_n * 2 * block_bytes * 2                 # K and V, read + write
+    # the same kernel on 1024 pairs x 28 layers (1.8 GB moved, far beyond L2)
+    pairs_l = 1024
+    cow_l = torch.stack([perm[:pairs_l], perm[pairs_l:2 * pairs_l]], 1).to(dev)
+    t_cow_l = timed(lambda: pa.pa_copy_blocks_layers(ks, vs, cow_l), 10)
+    cow_l_bytes = L * pairs_l * 2 * block_bytes * 2
     peak, src_peak = measured_peak()
     return {"metric": "block copies: swap through pinned host memory and all-layer copy-on-write",
             "component": "block_copy", "unit": "GB/s", "higher_is_better": True,
@@ -641,6 +656,8 @@ def run_block_copy(args) -> dict:
             "contiguous_d2h_gbs": moved / t_flat_out / 1e9, "contiguous_h2d_gbs": moved / t_flat_in / 1e9,
             "swap_out_frac_of_contiguous": t_flat_out / t_out, "swap_in_frac_of_contiguous": t_flat_in / t_in,
             "cow_all_layers_us": t_cow * 1e6, "cow_all_layers_gbs": cow_bytes / t_cow / 1e9,
+            "copy_1024_pairs_28_layers_us": t_cow_l * 1e6, "copy_1024_pairs_28_layers_gbs": cow_l_bytes / t_cow_l / 1e9,
+            "copy_1024_pairs_28_layers_frac": cow_l_bytes / t_cow_l / 1e9 / peak,
             "roofline": {"bound": "hbm", "kernel": "block_copy_kernel (28-layer COW)",
                          "achieved": cow_bytes / t_cow / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": cow_bytes / t_cow / 1e9 / peak, "peak_source": src_peak, "traffic": None}}

@@ -99,15 +99,22 @@ def test_profile_traffic_only_for_current_sources(monkeypatch, tmp_path):
         "x\nsource_sha256: abcdef0123456789\ntraffic_bytes_per_launch: 12345\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "source_digest", lambda: "abcdef0123456789")
-    assert bench.profile_traffic("w") == 12345
+    assert bench.profile_name("w") == "pa_decode_w"
+    assert bench.profile_traffic(bench.profile_name("w")) == 12345
     monkeypatch.setattr(bench, "source_digest", lambda: "0000000000000000")
-    assert bench.profile_traffic("w") is None            # kernels changed since the capture
-    assert bench.profile_traffic("missing") is None
+    assert bench.profile_traffic("pa_decode_w") is None      # kernels changed since the capture
+    assert bench.profile_traffic("pa_decode_missing") is None
+
+
+def test_profile_names_follow_the_configuration():
+    assert bench.profile_name("long_ctx_fp8", 512) == "pa_decode_long_ctx_fp8_p512"
+    assert bench.profile_name("qwen7b_fp16", 0, 8) == "pa_attention_qwen7b_fp16_q8"
+    assert bench.profile_name("qwen7b_fp16") == "pa_decode_qwen7b_fp16"
 
 
 def test_committed_profiles_name_their_digest_and_traffic():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    names = [n for n in os.listdir(os.path.join(root, "profiles")) if n.startswith("pa_decode_")]
+    names = [n for n in os.listdir(os.path.join(root, "profiles")) if n.startswith(("pa_decode_", "pa_attention_"))]
     assert names
     for n in names:
         txt = open(os.path.join(root, "profiles", n)).read()
