@@ -92,10 +92,10 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profile_name(workload: str, partition_tokens: int = 0, q_per_seq: int = 1) -> str:
+def profile_name(workload: str, partition_tokens: int = 0, q_per_seq: int = 1, simt: bool = False) -> str:
     """File stem of the committed ncu summary of one bench configuration."""
     stem = f"pa_attention_{workload}_q{q_per_seq}" if q_per_seq > 1 else f"pa_decode_{workload}"
-    return stem + (f"_p{partition_tokens}" if partition_tokens else "")
+    return stem + ("_simt" if simt else "") + (f"_p{partition_tokens}" if partition_tokens else "")
 
 
 def profile_traffic(name: str):
@@ -510,8 +510,8 @@ def run_ours(args, rank, world, local) -> dict | None:
                         "kernel": "pa_decode (main + reduce)" if NQ == 1 else "pa_attention (main + reduce)",
                         "algorithmic_bytes_per_launch": alg,
                         "launch_ms": dec_ms, "launch_ms_stat": f"median of {n_eager} eager calls",
-                        "traffic": profile_traffic(profile_name(args.workload, args.partition_tokens, NQ)),
-                        "profile": f"profiles/{profile_name(args.workload, args.partition_tokens, NQ)}.md"},
+                        "traffic": profile_traffic(profile_name(args.workload, args.partition_tokens, NQ, args.simt)),
+                        "profile": f"profiles/{profile_name(args.workload, args.partition_tokens, NQ, args.simt)}.md"},
            "gpu_launches": K * (3 + (1 if pairs is not None else 0)),
            "clocks": clk, "e2e": e2e,
            "cache_write_us_per_step": write_us,

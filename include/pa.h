@@ -238,6 +238,11 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype kv_dtype,
  * n_i <= max_q_len, and max_q_len * (num_q_heads / num_kv_heads) <= 128.
  * Tensor cores only (f16, bf16 and fp8 caches); other arguments as for
  * pa_decode.  With every n_i = 1 the result equals pa_decode's.
+ * Kernels: with at least 48 rows per KV head (max_q_len * G), a 16-bit cache
+ * and partition_tokens a multiple of 32, the rows of up to four KV heads
+ * (each padded to a multiple of 32) fill one 128-row tcgen05 tile whose S and
+ * O accumulators live in tensor memory (32-token chunks, P rounded to the
+ * cache's 16-bit type); otherwise 16-row mma.sync tiles as in pa_decode.
  */
 size_t pa_attention_workspace_size(int num_seqs, int max_q_len, int num_q_heads, int max_seq_len,
                                    int head_dim, int partition_tokens);

@@ -110,6 +110,7 @@ def test_profile_names_follow_the_configuration():
     assert bench.profile_name("long_ctx_fp8", 512) == "pa_decode_long_ctx_fp8_p512"
     assert bench.profile_name("qwen7b_fp16", 0, 8) == "pa_attention_qwen7b_fp16_q8"
     assert bench.profile_name("qwen7b_fp16") == "pa_decode_qwen7b_fp16"
+    assert bench.profile_name("qwen7b_fp16", simt=True) == "pa_decode_qwen7b_fp16_simt"
 
 
 def test_committed_profiles_name_their_digest_and_traffic():
