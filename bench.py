@@ -83,12 +83,20 @@ DECODE_SOURCES = ("pa_api.cu", "pa_common.h", "pa_decode_e4m3.cu", "pa_decode_ke
                   "pa_decode_tc.cu", "pa_device.cuh", "pa_kernels.h")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments or trailing blanks: the digest follows
+    what is compiled, not the prose around it."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     for name in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_69_gb300", "csrc", name), "rb") as f:
+        with open(os.path.join(ROOT, "paged_kv_cache_69_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

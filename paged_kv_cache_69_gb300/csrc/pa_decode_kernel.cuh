@@ -7,19 +7,24 @@
 // table, load block by block, merge across blocks with online softmax).
 //
 // How (GB300 design):
-//  * Work unit = a 16-token chunk of one sequence for HPC KV heads.  The
-//    chunks of all sequences form one stream that is cut into NR equal
-//    ranges, one per persistent CTA (times NHG head groups), so every CTA
-//    moves the same number of bytes whatever the length mix.
+//  * Work unit = a 16-token chunk (32 on the fp8 and tcgen05 paths) of one
+//    sequence for HPC KV heads.  The chunks of all sequences form one stream
+//    that is cut into NR ranges of equal cost (a chunk weighs WQ, a segment
+//    start WS more), one per persistent CTA (times NHG head groups), so every
+//    CTA does the same work whatever the length mix.
 //  * One producer warp per CTA walks its range, prefetches block-table
 //    entries 32 at a time into registers, and issues TMA tile loads of the
 //    K and V rows of each chunk (all HPC heads of a block in one copy, 128-B
-//    swizzled in shared memory) plus a bulk copy of the query rows at each
-//    segment start, into a ring of stages guarded by full/empty mbarriers.
+//    swizzled in shared memory) plus a copy of the query rows when it starts
+//    a sequence (at every segment start on the tcgen05 path), into a ring of
+//    stages guarded by full/empty mbarriers.
 //  * Consumer warps, one per (KV head, 16-row query tile), keep the GQA
 //    group's query heads packed as the M dimension of mma.sync m16n8k16
 //    (tensor-core variant) or as register rows (CUDA-core variant) and run
-//    online softmax over the chunk in fp32 (log2 domain).
+//    online softmax over the chunk in fp32 (log2 domain).  With 48 or more
+//    (query token, head) rows per KV head the rows of up to four KV heads
+//    fill a 128-row tcgen05 tile instead: one thread issues the MMAs into
+//    tensor memory, four warps run the softmax one row per thread.
 //  * A segment (the part of one sequence -- or of one partition of it --
 //    inside one CTA's range) ends by writing the final output directly when
 //    it covers the whole sequence, else an unnormalised partial
@@ -56,7 +61,7 @@ struct StageDesc {
     int slot;
     uint32_t vmask;
     uint32_t flags;          // SEG_* bits; bits 16.. hold the sequence's query count
-    int qslot;               // query ring slot of the segment's rows (valid at SEG_START chunks)
+    int qslot;               // query ring slot of the segment's rows (written at QLOAD chunks)
     int qrow0;               // row of the sequence's first query token in q / out
     int qpos0;               // its position in the sequence (queries are the last tokens)
 };
@@ -89,7 +94,7 @@ struct DecodeParams {
     int rpb;                  // rows per TMA box = min(16, bs)
     uint32_t box_bytes;       // bytes of one K (or V) box
     uint32_t kv_bytes;        // bytes of one stage's K (or V) buffer
-    uint32_t q_bytes;         // query bytes copied per segment start
+    uint32_t q_bytes;         // query bytes copied per query load
     uint32_t q_slot_bytes;    // one query ring slot
     uint32_t stage_bytes;     // K + V
     uint32_t q_off;           // offset of the query ring

@@ -120,3 +120,11 @@ def test_committed_profiles_name_their_digest_and_traffic():
     for n in names:
         txt = open(os.path.join(root, "profiles", n)).read()
         assert "source_sha256:" in txt and "traffic_bytes_per_launch:" in txt, n
+
+
+def test_source_digest_follows_code_not_comments():
+    a = "int f(int x) {  // doubles\n    return 2 * x; /* fast */\n}\n"
+    b = "// a header line\nint f(int x) {\n    return 2 * x;\n}\n"
+    c = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
