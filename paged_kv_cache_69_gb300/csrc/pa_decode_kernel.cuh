@@ -1683,10 +1683,19 @@ struct DecodeKernel {
         const uint32_t grp = p.rpb == 8 ? p.box_bytes : 1024u;
         const uint32_t dhs = static_cast<uint32_t>(HPC * p.rpb) * 128u;
         const uint32_t pb0 = smem_u32(base + p.simtq_off);
-        // byte offset of head h's token t0 (a multiple of 8) in a stage's K or V buffer
-        auto tok_off = [&](int t0, int h) -> uint32_t {
-            return static_cast<uint32_t>(t0 / p.rpb) * p.box_bytes + static_cast<uint32_t>(h * p.rpb + t0 % p.rpb) * 128u;
-        };
+        // byte offset of head h's 16-token group g in a stage's K or V buffer,
+        // worked out once: a division per MMA on this single issuing thread
+        // would stand between the consumers' P and the P V it waits for
+        constexpr int NG = CT / 16;
+        uint32_t toff[NG][4];
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int t0 = 16 * g;
+                toff[g][h] = static_cast<uint32_t>(t0 / p.rpb) * p.box_bytes +
+                             static_cast<uint32_t>(h * p.rpb + t0 % p.rpb) * 128u;
+            }
         bool ok = true;
         int q_cur = 0;          // query ring slot of the current segment (descriptors name it at its first chunk)
         // S of chunk st, its stage already landed
@@ -1698,9 +1707,11 @@ struct DecodeKernel {
             const uint32_t kb = smem_u32(base + slot * p.stage_bytes);
             const uint32_t sb = tm + (st & 1) * sspan;
             const int nmma = multi ? nbox : CT / 16;
-            for (int m = 0; m < nmma; ++m) {
+#pragma unroll
+            for (int m = 0; m < CT / 8; ++m) {       // at most CT / 8 boxes (8-row boxes)
+                if (m >= nmma) break;
                 // multi: box m, all heads (columns m * HPC * rpb ..); else tokens 16m .. 16m + 15
-                const uint32_t kbase = multi ? kb + static_cast<uint32_t>(m) * p.box_bytes : kb + tok_off(16 * m, 0);
+                const uint32_t kbase = multi ? kb + static_cast<uint32_t>(m) * p.box_bytes : kb + toff[m & (NG - 1)][0];
                 const uint32_t dcol = multi ? static_cast<uint32_t>(m * HPC * p.rpb) : static_cast<uint32_t>(16 * m);
                 const uint32_t ksbo = multi ? 1024u : grp;
 #pragma unroll
@@ -1740,13 +1751,15 @@ struct DecodeKernel {
             if (first) ++seg;
             tc05_fence_after();
             const uint32_t vb = smem_u32(base + slot * p.stage_bytes + p.kv_bytes);
-            for (int h = 0; h < HPC; ++h) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (h >= HPC) break;
                 const uint32_t pbh = pb0 + static_cast<uint32_t>((st & 1) * HPC + h) * UM_PBUF;
 #pragma unroll
-                for (int k16 = 0; k16 < CT / 16; ++k16)
+                for (int k16 = 0; k16 < NG; ++k16)
                     umma_f16(tm + ocol,
                              umma_desc(pbh + k16 * 2u * (UM_M / 8) * 128u, (UM_M / 8) * 128u, 128u, 0u),
-                             umma_desc(vb + tok_off(16 * k16, h), dhs, grp, 2u), id_o, !first || h > 0 || k16 > 0);
+                             umma_desc(vb + toff[k16][h], dhs, grp, 2u), id_o, !first || h > 0 || k16 > 0);
             }
             umma_commit(&ub->pvdone[st & 1]);
             umma_commit(&empty[slot]);                                 // K and V of the stage are read
