@@ -89,10 +89,11 @@ static CUtensorMapDataType tmap_type(pa_dtype d) {
 // shared memory as [column block of 128 B][head][row][128 B] with the 128-B
 // swizzle.  The 4-D map lists the dimensions in that shared-memory order
 // (column-in-block, row, head, column block), so one copy moves the box.
-// Fallback: a 3-D map in the pool's natural order, one copy per
-// (column block, head).
+// With one_plane the box holds a single column block (the tcgen05 path places
+// each block separately).  Fallback: a 3-D map in the pool's natural order,
+// one copy per (column block, head).
 static CUresult encode_kv_map(CUtensorMap* m, const void* cache, pa_dtype kvd, int NB, int bs, int Hkv,
-                              int D, int HPC, int rpb, bool per_head) {
+                              int D, int HPC, int rpb, bool per_head, bool one_plane) {
     const EncodeTiledFn enc = encode_fn();
     if (!enc) return CUDA_ERROR_NOT_FOUND;
     const int e = dtype_bytes(kvd);
@@ -102,7 +103,7 @@ static CUresult encode_kv_map(CUtensorMap* m, const void* cache, pa_dtype kvd, i
     if (!per_head) {
         cuuint64_t dims[4] = {e128, rows, static_cast<cuuint64_t>(Hkv), DH};
         cuuint64_t strides[3] = {static_cast<cuuint64_t>(Hkv) * D * e, static_cast<cuuint64_t>(D) * e, 128};
-        cuuint32_t box[4] = {e128, static_cast<cuuint32_t>(rpb), static_cast<cuuint32_t>(HPC), DH};
+        cuuint32_t box[4] = {e128, static_cast<cuuint32_t>(rpb), static_cast<cuuint32_t>(HPC), one_plane ? 1u : DH};
         cuuint32_t es[4] = {1, 1, 1, 1};
         return enc(m, tmap_type(kvd), 4, const_cast<void*>(cache), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -336,12 +337,12 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     // tensor maps
     alignas(64) CUtensorMap tk, tv;
     p.per_head_copies = 0;
-    CUresult r1 = encode_kv_map(&tk, k_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, false);
-    CUresult r2 = r1 == CUDA_SUCCESS ? encode_kv_map(&tv, v_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, false) : r1;
+    CUresult r1 = encode_kv_map(&tk, k_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, false, um);
+    CUresult r2 = r1 == CUDA_SUCCESS ? encode_kv_map(&tv, v_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, false, um) : r1;
     if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
         p.per_head_copies = 1;
-        r1 = encode_kv_map(&tk, k_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, true);
-        r2 = r1 == CUDA_SUCCESS ? encode_kv_map(&tv, v_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, true) : r1;
+        r1 = encode_kv_map(&tk, k_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, true, um);
+        r2 = r1 == CUDA_SUCCESS ? encode_kv_map(&tv, v_cache, kv_dtype, NB, bs, Hkv, D, HPC, rpb, true, um) : r1;
         if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
             char msg[96];
             std::snprintf(msg, sizeof msg, "decode: cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r1 ? r1 : r2));

@@ -543,6 +543,29 @@ struct DecodeKernel {
                         if (b >= nb) break;
                         if (!((issue_mask >> b) & 1u)) continue;
                         const int row0 = blk[b] * p.bs + (p.bs > CT ? (tok0 % p.bs) : 0);
+                        if constexpr (UM) {
+                            // tcgen05 layout: column plane dh of box b at
+                            // (dh * nb + b) * pbox, so that one plane's rows of
+                            // every box of the chunk are contiguous (the N rows
+                            // of one S MMA)
+                            const uint32_t pbox = static_cast<uint32_t>(p.HPC * p.rpb) * 128u;
+#pragma unroll
+                            for (int dh = 0; dh < ROWB / 128; ++dh) {
+                                const uint32_t off = static_cast<uint32_t>(dh * nb + b) * pbox;
+                                if (!p.per_head_copies) {
+                                    tma_load_4d(kbuf + off, tk, &full[slot], 0, row0, hg * p.HPC, dh);
+                                    tma_load_4d(vbuf + off, tv, &full[slot], 0, row0, hg * p.HPC, dh);
+                                } else {
+                                    const int E128 = 128 / KV::bytes;
+                                    for (int hl = 0; hl < p.HPC; ++hl) {
+                                        const uint32_t o2 = off + static_cast<uint32_t>(hl * p.rpb) * 128u;
+                                        tma_load_3d(kbuf + o2, tk, &full[slot], dh * E128, hg * p.HPC + hl, row0);
+                                        tma_load_3d(vbuf + o2, tv, &full[slot], dh * E128, hg * p.HPC + hl, row0);
+                                    }
+                                }
+                            }
+                            continue;
+                        }
                         uint8_t* kd = kbuf + b * p.box_bytes;
                         uint8_t* vd = vbuf + b * p.box_bytes;
                         if (!p.per_head_copies) {
@@ -1485,8 +1508,10 @@ struct DecodeKernel {
         const uint32_t sspan = static_cast<uint32_t>(CT * p.HPC);   // columns of one S buffer
         const uint32_t ocol = 2u * sspan;                          // first column of O
         const int S = p.stages;
-        const KVLayout lay{p.box_bytes, static_cast<uint32_t>(p.rpb) * 128u,
-                           static_cast<uint32_t>(p.HPC * p.rpb) * 128u, p.rpb};
+        // stage layout of the tcgen05 path: column plane dh of box b at (dh * nbox + b) * pbox
+        const uint32_t pbox = static_cast<uint32_t>(p.HPC * p.rpb) * 128u;
+        const KVLayout lay{pbox, static_cast<uint32_t>(p.rpb) * 128u,
+                           static_cast<uint32_t>(CT / p.rpb) * pbox, p.rpb};
         uint8_t* pbuf0 = base + p.simtq_off;
         constexpr uint32_t FULLM = CT == 32 ? 0xffffffffu : ((1u << CT) - 1u);
         // P buffers start at zero: a head's buffer only ever gets its own
@@ -1674,14 +1699,16 @@ struct DecodeKernel {
         const uint32_t sspan = static_cast<uint32_t>(CT * HPC);
         const uint32_t ocol = 2u * sspan;
         const int nbox = CT / p.rpb;                      // TMA boxes per chunk
-        const bool multi = HPC > 1;
-        const uint32_t id_s = umma_idesc_f16(MMA_BF16, UM_M, multi ? HPC * p.rpb : 16, false, false);
+        // Stage layout: column plane dh of box b at (dh * nbox + b) * pbox,
+        // so a plane holds the chunk's rows (box, head, row) contiguously and
+        // S = Q K^T takes one MMA per k-step with N = CT * HPC.
+        const uint32_t pbox = static_cast<uint32_t>(HPC * p.rpb) * 128u;
+        const uint32_t dhs = static_cast<uint32_t>(nbox) * pbox;             // 64-element column planes apart
+        const uint32_t id_s = umma_idesc_f16(MMA_BF16, UM_M, CT * HPC, false, false);
         const uint32_t id_o = umma_idesc_f16(MMA_BF16, UM_M, D, false, true);
-        // 8-token groups of one head's K / V rows: 1024 B apart inside a box
-        // of 16 or more rows, one box apart with 8-row boxes; 64-element
-        // column blocks HPC * rpb * 128 B apart
-        const uint32_t grp = p.rpb == 8 ? p.box_bytes : 1024u;
-        const uint32_t dhs = static_cast<uint32_t>(HPC * p.rpb) * 128u;
+        // 8-token groups of one head's V rows: 1024 B apart inside a box of
+        // 16 or more rows, one box (pbox) apart with 8-row boxes
+        const uint32_t grp = p.rpb == 8 ? pbox : 1024u;
         const uint32_t pb0 = smem_u32(base + p.simtq_off);
         // byte offset of head h's 16-token group g in a stage's K or V buffer,
         // worked out once: a division per MMA on this single issuing thread
@@ -1693,7 +1720,7 @@ struct DecodeKernel {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const int t0 = 16 * g;
-                toff[g][h] = static_cast<uint32_t>(t0 / p.rpb) * p.box_bytes +
+                toff[g][h] = static_cast<uint32_t>(t0 / p.rpb) * pbox +
                              static_cast<uint32_t>(h * p.rpb + t0 % p.rpb) * 128u;
             }
         bool ok = true;
@@ -1706,20 +1733,12 @@ struct DecodeKernel {
             const uint32_t qb = smem_u32(base + p.q_off + q_cur * p.q_slot_bytes);
             const uint32_t kb = smem_u32(base + slot * p.stage_bytes);
             const uint32_t sb = tm + (st & 1) * sspan;
-            const int nmma = multi ? nbox : CT / 16;
+            // S column (b * HPC + h) * rpb + r holds token b * rpb + r of head h
 #pragma unroll
-            for (int m = 0; m < CT / 8; ++m) {       // at most CT / 8 boxes (8-row boxes)
-                if (m >= nmma) break;
-                // multi: box m, all heads (columns m * HPC * rpb ..); else tokens 16m .. 16m + 15
-                const uint32_t kbase = multi ? kb + static_cast<uint32_t>(m) * p.box_bytes : kb + toff[m & (NG - 1)][0];
-                const uint32_t dcol = multi ? static_cast<uint32_t>(m * HPC * p.rpb) : static_cast<uint32_t>(16 * m);
-                const uint32_t ksbo = multi ? 1024u : grp;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t plane = static_cast<uint32_t>(kk >> 2), within = static_cast<uint32_t>(kk & 3) * 32u;
-                    umma_f16(sb + dcol, umma_desc(qb + plane * p.q_plane_bytes + within, 16u, 1024u, 2u),
-                             umma_desc(kbase + plane * dhs + within, 16u, ksbo, 2u), id_s, kk > 0);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t plane = static_cast<uint32_t>(kk >> 2), within = static_cast<uint32_t>(kk & 3) * 32u;
+                umma_f16(sb, umma_desc(qb + plane * p.q_plane_bytes + within, 16u, 1024u, 2u),
+                         umma_desc(kb + plane * dhs + within, 16u, 1024u, 2u), id_s, kk > 0);
             }
             umma_commit(&ub->sfull[st & 1]);
             if (d.flags & SEG_END) umma_commit(&qempty[q_cur]);       // the segment's query rows are read
