@@ -283,7 +283,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     const uint32_t simtq = um ? 2u * static_cast<uint32_t>(HPC) * 128u * static_cast<uint32_t>(CT) * 2u
                          : fp8t ? static_cast<uint32_t>(NCW * 256) : tc ? 0u : static_cast<uint32_t>(NCW * 16 * D * 4);
     const uint32_t extras = 1024;   // barriers, stage descriptors, prologue scratch
-    const uint32_t fixed = NQ * p.q_slot_bytes + simtq + extras + 1024;   // + base alignment slack
+    const uint32_t fixed = nq_slots(um) * p.q_slot_bytes + simtq + extras + 1024;   // + base alignment slack
     const int threads = (NCW + (um ? 2 : 1)) * 32;
     // Two co-resident CTAs per SM double the consumer warps that hide the
     // per-chunk MMA/softmax latency; use them when registers and shared
@@ -314,7 +314,7 @@ static pa_status decode_impl(bool tc, void* out, const void* q, pa_dtype q_dtype
     if (stages < 2) return fail(PA_ERR_UNSUPPORTED, "decode: pipeline stages do not fit in shared memory");
     p.stages = stages;
     p.q_off = stages * p.stage_bytes;
-    p.simtq_off = p.q_off + NQ * p.q_slot_bytes;
+    p.simtq_off = p.q_off + nq_slots(um) * p.q_slot_bytes;
     p.bar_off = (p.simtq_off + simtq + 15u) & ~15u;
     const size_t smem = 1024 + p.bar_off + extras;
     const float log2e = 1.4426950408889634f;

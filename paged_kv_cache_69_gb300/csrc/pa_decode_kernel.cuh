@@ -43,6 +43,9 @@ namespace pa {
 
 constexpr int MAX_STAGES = 8;
 constexpr int NQ = 2;                // query-row ring slots
+// The tcgen05 path's query tile (128 rows x head_dim) is 32 KB: one slot
+// there leaves room for one more K/V stage.
+constexpr int nq_slots(bool um) { return um ? 1 : NQ; }
 constexpr int MAX_WARPS = 9;         // up to 8 consumers + 1 producer
 
 // GAP: this segment ends the CTA's range exactly at a partition end while
@@ -525,11 +528,11 @@ struct DecodeKernel {
                 d.seq = i; d.tok0 = tok0; d.vmask = vmask;
                 d.flags = flags | (static_cast<uint32_t>(qn_i) << QCOUNT_SHIFT);
                 d.slot = range + Ui + ju;
-                d.qslot = qload ? qs : (qs == 0 ? NQ - 1 : qs - 1);
+                d.qslot = qload ? qs : (qs == 0 ? nq_slots(UM) - 1 : qs - 1);
                 d.qrow0 = qrow_i;
                 d.qpos0 = L - qn_i;
                 const uint32_t bytes = nbox_issued * p.box_bytes * 2u + (qload ? p.q_bytes : 0u);
-                if (ok && qload && qcount >= NQ && !mbar_wait_bounded(&qempty[qs], (qround - 1) & 1u)) {
+                if (ok && qload && qcount >= nq_slots(UM) && !mbar_wait_bounded(&qempty[qs], (qround - 1) & 1u)) {
                     raise_flag(p.err_flag, PA_ERRBIT_WAIT_TIMEOUT);
                     ok = false;
                 }
@@ -604,7 +607,7 @@ struct DecodeKernel {
                             else bulk_load(qdst, qsrc, p.q_bytes, &full[slot]);
                         }
                         ++qcount;
-                        if (++qs == NQ) { qs = 0; ++qround; }
+                        if (++qs == nq_slots(UM)) { qs = 0; ++qround; }
                     }
                 }
             }
